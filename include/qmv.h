@@ -1,0 +1,197 @@
+/*
+ * qmv.h -- C ABI of libqmv: low-bit weight-quantized matrix-vector and
+ * matrix-matrix products for LLM inference on GB300 (sm_103a).
+ *
+ * Formats (as defined by the pages the method comes from):
+ *
+ *  q8_row   int8 codes q[rows][cols] plus one f32 scale per row:
+ *             y[o] = rs[o] * sum_i q[o,i] * xs[i]
+ *           xs is already multiplied by the per-column field of the
+ *           two-field variant, so the library never sees that field.
+ *           (cortiq-engine 0.5.43 src/gpu_wgpu.rs, module doc comment and
+ *           WGSL `q8_matvec`; cortiq-engine 0.3.7 src/gpu_metal.rs, MSL
+ *           `q8_matvec`.)
+ *
+ *  Q2 g64 / g128   2-bit codes, four per byte, code k of a row in byte k/4
+ *           at bits 2(k%4); one f16 scale d per group of 64 or 128 weights;
+ *             w[m,k] = d[m, k/G] * (q[m,k] - 1),   q in {0,1,2,3}
+ *           (qxmx_gpu.cpp, `dequant_embd`; block footprints in `upload_q2`.)
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer (memory the caller owns,
+ *    e.g. from PyTorch) unless its comment says "host".
+ *  - Work is enqueued on the caller's stream `st` (NULL = the legacy
+ *    default stream).  No entry point synchronizes; the caller does.
+ *  - All arguments are validated before anything is enqueued.  On any error
+ *    the call returns a non-zero qmv_status and enqueues nothing (there is
+ *    no CPU fallback).  qmv_last_error() then gives a one-line reason.
+ *  - Outputs must not alias inputs.
+ *  - Packed weights (qmv_weights) are owned by the library; the caller frees
+ *    them with qmv_weights_free() after all work that reads them is done.
+ *  - Thread safety: calls that read a handle may run concurrently; packing
+ *    and freeing a handle need external ordering.
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *qmv_stream;
+
+typedef enum {
+    QMV_OK = 0,
+    QMV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+    QMV_ERR_UNSUPPORTED = 2,   /* valid arguments outside what a kernel covers,
+                                  or a handle of the wrong format */
+    QMV_ERR_ALLOC = 3,         /* device allocation failed */
+    QMV_ERR_CUDA = 4,          /* a CUDA call or launch failed */
+    QMV_ERR_DEVICE_STATUS = 5  /* a kernel reported a violated invariant */
+} qmv_status;
+
+typedef enum {
+    QMV_FMT_Q8ROW = 1,
+    QMV_FMT_Q2G64 = 2,
+    QMV_FMT_Q2G128 = 3
+} qmv_format;
+
+typedef struct qmv_weights qmv_weights; /* opaque, library-owned */
+
+/* Static, never-NULL name of a status code. */
+const char *qmv_status_string(int status);
+
+/* Copies the calling thread's last error message (host buffer `buf` of `n`
+ * bytes, always NUL-terminated when n > 0).  Returns the status it belongs to. */
+int qmv_last_error(char *buf, size_t n);
+
+/* ABI version (major * 100 + minor). */
+int qmv_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* Load-time repack (done once per weight tensor; not on the per-token path) */
+/* ---------------------------------------------------------------------- */
+
+/* Packs q8_row weights into the library's layout.
+ *   q   [experts][rows][cols] int8, row-major      (device, read only)
+ *   rs  [experts][rows] f32                         (device, read only)
+ *   experts >= 1: number of stacked matrices of the same shape (MoE expert
+ *   stacks; 1 for a plain matrix).  rows >= 1, cols >= 16, cols % 16 == 0.
+ * The repack runs on `st`; `q` and `rs` must stay valid until it completes.
+ * Writes a new handle to *out (host pointer).
+ * (Repack at load time: qxmx_gpu.cpp, `upload_q2`, which reorders the
+ * weights once at upload so that the hot loop reads them in order.) */
+qmv_status qmv_pack_q8row(const int8_t *q, const float *rs, int64_t experts,
+                          int64_t rows, int64_t cols, qmv_stream st,
+                          qmv_weights **out);
+
+/* Packs 2-bit group weights (planar form).
+ *   codes [rows][cols/4] bytes; code k of row m is (codes[m][k/4] >> 2(k%4)) & 3
+ *   d     [rows][cols/group] IEEE f16 bit patterns
+ *   group 64 or 128; cols % group == 0; rows >= 1.
+ * Same ownership rules as qmv_pack_q8row.
+ * (qxmx_gpu.cpp, `dequant_embd` for the bit order, `repack_q2_g64`,
+ * `repack_q2_g128` and `upload_q2` for the load-time repack.) */
+qmv_status qmv_pack_q2(const uint8_t *codes, const uint16_t *d, int group,
+                       int64_t rows, int64_t cols, qmv_stream st,
+                       qmv_weights **out);
+
+/* Describes a handle (host out-pointers, each may be NULL). */
+qmv_status qmv_weights_info(const qmv_weights *w, int *format, int64_t *experts,
+                            int64_t *rows, int64_t *cols, int64_t *device_bytes);
+
+/* Frees a handle (NULL is a no-op).  Synchronizes the device first, so
+ * work already enqueued that reads the handle completes. */
+qmv_status qmv_weights_free(qmv_weights *w);
+
+/* ---------------------------------------------------------------------- */
+/* Decode GEMVs                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* y[o] = rs[o] * sum_i q[o,i] * xs[i] for a q8_row handle with experts == 1.
+ *   xs [cols] f32, y [rows] f32, both 16-byte aligned.
+ * fp32 arithmetic on exactly converted int8 codes; deterministic.
+ * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `q8_matvec`; cortiq-engine
+ * 0.3.7 src/gpu_metal.rs, MSL `q8_matvec`.) */
+qmv_status qmv_q8row(const qmv_weights *w, const float *xs, float *y,
+                     qmv_stream st);
+
+/* y[m] = sum_g d[m,g] * sum_{k in g} (q[m,k] - 1) * x[k] for a Q2 g64
+ * (qmv_q2g64) or g128 (qmv_q2g128) handle; a handle of the other group
+ * size returns QMV_ERR_UNSUPPORTED.
+ *   x [cols] f32, y [rows] f32, both 16-byte aligned.  cols <= 32768.
+ * The K dimension is split across warps and the partial sums are reduced
+ * in a fixed order (deterministic).
+ * (qxmx_gpu.cpp, `gemv_dpas8` and its split-K reduce `gemv_reduce`.) */
+qmv_status qmv_q2g64(const qmv_weights *w, const float *x, float *y,
+                     qmv_stream st);
+qmv_status qmv_q2g128(const qmv_weights *w, const float *x, float *y,
+                      qmv_stream st);
+
+/* ---------------------------------------------------------------------- */
+/* Prefill GEMM                                                           */
+/* ---------------------------------------------------------------------- */
+
+/* y[b,o] = rs[o] * sum_i q[o,i] * xs[b,i] for a q8_row handle (experts == 1).
+ *   xs [nb][cols] f32 row-major, y [nb][rows] f32 row-major, nb >= 1,
+ *   both 16-byte aligned.
+ * Tensor-core path: int8 codes become bf16 exactly, xs is rounded to bf16
+ * (nearest even), products accumulate in fp32, rs is applied to the fp32
+ * result.  Uses a stream-ordered scratch allocation of nb*cols*2 bytes.
+ * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `q8_matmat` and `q8_mul_mm`;
+ * cortiq-engine 0.3.7 src/gpu_metal.rs, MSL `q8_mul_mm`.) */
+qmv_status qmm_q8row(const qmv_weights *w, const float *xs, int64_t nb,
+                     float *y, qmv_stream st);
+
+/* ---------------------------------------------------------------------- */
+/* MoE                                                                    */
+/* ---------------------------------------------------------------------- */
+
+/* Router select for one token.
+ *   logits [n_exp] f32 (finite), 1 <= top_k <= n_exp <= 1024.
+ *   Softmax over all n_exp logits; top_k rounds of argmax over the logits
+ *   (equal values: the lowest index wins); w[s] = exp(l_sel - max) / sum;
+ *   renorm != 0 divides the top_k weights by their sum.
+ *   Shared expert: if sg_w != NULL, gate = sum_i sg_w[i] * x[i] over
+ *   `hidden` values; else if sg_logit != NULL (device, one f32), gate =
+ *   *sg_logit; then sel[top_k] = n_exp and w[top_k] = 1/(1+exp(-gate)).
+ *   If both are NULL there is no shared slot.
+ *   Outputs: sel [top_k(+1)] int32, w [top_k(+1)] f32.
+ * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_select_sg` and
+ * `moe_select`.) */
+qmv_status moe_select_topk(const float *logits, int n_exp, int top_k,
+                           int renorm, const float *sg_w, const float *x,
+                           int hidden, const float *sg_logit, int32_t *sel,
+                           float *w, qmv_stream st);
+
+/* Expert FFN over `slots` selected experts (routed + shared):
+ *   g_s = gate[e_s] x, u_s = up[e_s] x (q8_row, rs applied), act_s = silu(g_s)*u_s,
+ *   out[h] = sum_s w[s] * (down[e_s] act_s)[h],     e_s = sel[s].
+ * gate/up: q8_row handles with experts = E, rows = inter, cols = hidden;
+ * down: experts = E, rows = hidden, cols = inter.  sel [slots] int32 in
+ * [0, E) (device; an out-of-range id makes the kernel skip that slot and
+ * report QMV_ERR_DEVICE_STATUS on the next qmv_check()), w [slots] f32,
+ * x [hidden] f32, out [hidden] f32.  1 <= slots <= 64.
+ * Uses a stream-ordered scratch allocation of slots*inter*4 bytes.
+ * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_gate_up` and `moe_down`;
+ * cortiq-engine 0.3.7 src/gpu_metal.rs, host `moe_block`.) */
+qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
+                         const qmv_weights *down, const int32_t *sel,
+                         const float *w, int slots, const float *x,
+                         float *out, qmv_stream st);
+
+/* Reads and clears the device status word that kernels set when they meet
+ * a violated invariant (e.g. an expert id out of range).  Synchronizes `st`.
+ * Returns QMV_OK or QMV_ERR_DEVICE_STATUS (*code gets the first reason,
+ * host pointer, may be NULL). */
+qmv_status qmv_check(qmv_stream st, int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H */

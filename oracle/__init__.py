@@ -1,0 +1,204 @@
+"""fp64 CPU oracle for the quantized GEMV/GEMM hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The library under
+``gemm_decode_prefill_gb300/`` never does, and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, one thread per row
+block); this module only compiles it with gcc and marshals numpy arrays.
+Which passage of the pages each function follows is stated in ``oracle.c``.
+Pins that fix the oracle independently of itself: ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+# A test may point the wrapper at a deliberately mutated build of oracle.c
+# (tests/test_oracle_mutations.py) to show that the pins catch the mutation.
+_OVERRIDE = os.environ.get("QMV_ORACLE_LIB_OVERRIDE")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, no FP contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm",
+        ])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if _OVERRIDE:
+        lib = ctypes.CDLL(_OVERRIDE)
+    else:
+        build()
+        lib = ctypes.CDLL(_LIB)
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    I = ctypes.c_int
+    lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_f16_to_f64.restype = ctypes.c_double
+    lib.oracle_round_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_round_bf16.restype = ctypes.c_float
+    lib.oracle_threads.argtypes = [I, I64]
+    lib.oracle_threads.restype = I
+    lib.oracle_q8row.argtypes = [P, P, P, I64, I64, P, P, I]
+    lib.oracle_q8row.restype = I
+    lib.oracle_qmm.argtypes = [P, P, P, I64, I64, I64, P, P, I]
+    lib.oracle_qmm.restype = I
+    lib.oracle_qmm_bf16.argtypes = [P, P, P, I64, I64, I64, P, P, I]
+    lib.oracle_qmm_bf16.restype = I
+    lib.oracle_q2.argtypes = [P, P, I, P, I64, I64, P, P, I]
+    lib.oracle_q2.restype = I
+    lib.oracle_select.argtypes = [P, I, I, I, P, P, I, P, P, P]
+    lib.oracle_select.restype = I
+    lib.oracle_moe_ffn.argtypes = [P, P, P, P, P, P, I64, I64, I64, P, P, I,
+                                   P, P, P, P, P, P]
+    lib.oracle_moe_ffn.restype = I
+    _lib = lib
+    return lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def threads(want: int = 0, rows: int = 1 << 30) -> int:
+    """Threads a call with ``nthreads=want`` uses (0: all online cores)."""
+    return _load().oracle_threads(want, rows)
+
+
+def f16_to_f64(bits: int) -> float:
+    return _load().oracle_f16_to_f64(int(bits) & 0xFFFF)
+
+
+def round_bf16(x: float) -> float:
+    return _load().oracle_round_bf16(float(x))
+
+
+def q8row(q, rs, xs, nthreads: int = 0, with_mag: bool = False):
+    """y[o] = rs[o] * sum_i q[o,i] xs[i] in fp64.  q: [rows][cols] int8."""
+    lib = _load()
+    q, qp = _c(q, np.int8)
+    rows, cols = q.shape
+    rs, rsp = _c(rs, np.float32)
+    xs, xsp = _c(xs, np.float32)
+    assert rs.shape == (rows,) and xs.shape == (cols,)
+    y = np.empty(rows, np.float64)
+    mag = np.empty(rows, np.float64) if with_mag else None
+    lib.oracle_q8row(qp, rsp, xsp, rows, cols, y.ctypes.data,
+                     mag.ctypes.data if with_mag else None, nthreads)
+    return (y, mag) if with_mag else y
+
+
+def qmm(q, rs, xs, nthreads: int = 0, with_mag: bool = False, bf16_xs: bool = False):
+    """y[b,o] = rs[o] * sum_i q[o,i] xs[b,i]; returns [nb][rows] fp64.
+
+    ``bf16_xs`` selects the diagnostic twin (xs rounded to bf16 first)."""
+    lib = _load()
+    q, qp = _c(q, np.int8)
+    rows, cols = q.shape
+    rs, rsp = _c(rs, np.float32)
+    xs, xsp = _c(xs, np.float32)
+    nb = xs.shape[0]
+    assert rs.shape == (rows,) and xs.shape == (nb, cols)
+    y = np.empty((nb, rows), np.float64)
+    mag = np.empty((nb, rows), np.float64) if with_mag else None
+    fn = lib.oracle_qmm_bf16 if bf16_xs else lib.oracle_qmm
+    fn(qp, rsp, xsp, nb, rows, cols, y.ctypes.data,
+       mag.ctypes.data if with_mag else None, nthreads)
+    return (y, mag) if with_mag else y
+
+
+def q2(codes, d_bits, group: int, x, nthreads: int = 0, with_mag: bool = False):
+    """Q2 group GEMV in fp64.  codes: [rows][cols/4] uint8 (code k at byte
+    k/4, bits 2(k%4)); d_bits: [rows][cols/group] f16 bit patterns (uint16)."""
+    lib = _load()
+    if group not in (64, 128):
+        raise ValueError("oracle_q2: group must be 64 or 128")
+    codes, cp = _c(codes, np.uint8)
+    rows = codes.shape[0]
+    cols = codes.shape[1] * 4
+    d_bits, dp = _c(d_bits, np.uint16)
+    x, xp = _c(x, np.float32)
+    assert d_bits.shape == (rows, cols // group) and x.shape == (cols,)
+    y = np.empty(rows, np.float64)
+    mag = np.empty(rows, np.float64) if with_mag else None
+    rc = lib.oracle_q2(cp, dp, group, xp, rows, cols, y.ctypes.data,
+                       mag.ctypes.data if with_mag else None, nthreads)
+    if rc < 0:
+        raise ValueError("oracle_q2: bad group/cols")
+    return (y, mag) if with_mag else y
+
+
+def select(logits, top_k: int, renorm: bool, sgw=None, x=None, sg_logit=None):
+    """Router select.  Returns (sel int32 [k or k+1], w float64)."""
+    lib = _load()
+    logits, lp = _c(logits, np.float32)
+    n = logits.shape[0]
+    slots = top_k + (1 if (sgw is not None or sg_logit is not None) else 0)
+    sel = np.zeros(max(slots, 1), np.int32)
+    w = np.zeros(max(slots, 1), np.float64)
+    hidden = 0
+    sgp = xp = slp = None
+    keep = []
+    if sgw is not None:
+        sgw, sgp = _c(sgw, np.float32)
+        x, xp = _c(x, np.float32)
+        hidden = sgw.shape[0]
+        keep += [sgw, x]
+    elif sg_logit is not None:
+        slv, slp = _c(np.array([sg_logit], np.float32), np.float32)
+        keep.append(slv)
+    got = lib.oracle_select(lp, n, top_k, int(bool(renorm)), sgp, xp, hidden, slp,
+                            sel.ctypes.data, w.ctypes.data)
+    if got < 0:
+        raise ValueError("oracle_select: bad arguments")
+    return sel[:got], w[:got]
+
+
+def moe_ffn(gq, grs, uq, urs, dq, drs, sel, w, x, with_parts: bool = False):
+    """MoE expert FFN over the selected slots in fp64.
+
+    gq/uq: [E][inter][hidden] int8, grs/urs: [E][inter]; dq: [E][hidden][inter]
+    int8, drs: [E][hidden]; sel: [slots] expert ids; w: [slots] weights.
+    Returns out [hidden] (and, with_parts, a dict of g, u, act, mag)."""
+    lib = _load()
+    gq, gqp = _c(gq, np.int8)
+    uq, uqp = _c(uq, np.int8)
+    dq, dqp = _c(dq, np.int8)
+    E, inter, hidden = gq.shape
+    assert uq.shape == gq.shape and dq.shape == (E, hidden, inter)
+    grs, grp = _c(grs, np.float32)
+    urs, urp = _c(urs, np.float32)
+    drs, drp = _c(drs, np.float32)
+    sel, sp = _c(sel, np.int32)
+    w, wp = _c(w, np.float64)
+    x, xp = _c(x, np.float32)
+    slots = sel.shape[0]
+    out = np.empty(hidden, np.float64)
+    g = np.empty((slots, inter)); u = np.empty((slots, inter))
+    act = np.empty((slots, inter)); mag = np.empty(hidden)
+    rc = lib.oracle_moe_ffn(gqp, grp, uqp, urp, dqp, drp, E, inter, hidden, sp, wp,
+                            slots, xp, out.ctypes.data, g.ctypes.data, u.ctypes.data,
+                            act.ctypes.data, mag.ctypes.data)
+    if rc < 0:
+        raise ValueError("oracle_moe_ffn: expert index out of range")
+    if with_parts:
+        return out, {"g": g, "u": u, "act": act, "mag": mag}
+    return out

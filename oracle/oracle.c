@@ -1,0 +1,405 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for the quantized GEMV/GEMM
+ * hot path.  TEST INFRASTRUCTURE ONLY: it is called by tests/, by
+ * __graft_entry__.smoke() and by bench.py's CPU-baseline leg, never by the
+ * library.  It shares no code, header or table with the CUDA path.
+ *
+ * Every function is the plain definition written out: the inputs are the
+ * exact stored values (int8 codes, f32 scales and activations, f16 group
+ * scales, 2-bit codes), every product is formed exactly in double and every
+ * sum is taken left to right in double.  Rows are split across POSIX threads;
+ * that changes no arithmetic (each row is summed by one thread, in order).
+ *
+ * Sources (the pages the method is taken from):
+ *  [P1] qxmx_gpu.cpp (tangled.org/clee.sh/qxmx, branch extra-debug):
+ *       `dequant_embd` (Q2 code k at byte k/4, bits 2(k%4); w = d*(q-1)),
+ *       the `qx_block_q2` / `qx_block_q2_g128` footprints in `upload_q2`
+ *       (18 B per 64 weights, 34 B per 128), `repack_q2_g128` (one g128
+ *       block = two g64 blocks that share d).
+ *  [P2] cortiq-engine 0.5.43, src/gpu_wgpu.rs: module doc comment
+ *       (y[o] = row_scale[o] * sum_i q[o,i]*xs[i], xs already prescaled),
+ *       WGSL `q8_matvec`, `q8_matmat` (y[bi,o] layout [nb][rows]),
+ *       `moe_select_sg` / `moe_select` (softmax over all n_exp logits, k rounds
+ *       of argmax with the lowest index winning ties, optional renormalisation
+ *       by the selected sum, shared expert pinned at slot k with a sigmoid
+ *       weight), `moe_gate_up` (act = silu(g)*u), `moe_down`
+ *       (sum over slots of w[slot] * down[sel[slot]] row . act[slot]).
+ *  [P3] cortiq-engine 0.3.7, src/gpu_metal.rs: MSL `q8_matvec`, `q8_matmat`,
+ *       host `moe_block` (per expert: gate/up matvec -> silu*mul -> down
+ *       matvec -> y += w*d).
+ *
+ * Parity pins (what fixes each function independently of itself) live in
+ * tests/test_oracle_pins.py.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* ------------------------------------------------------------------------ */
+/* Scalar decoders, written from the IEEE-754 definitions.                  */
+/* ------------------------------------------------------------------------ */
+
+/* IEEE-754 binary16 -> double, exactly.  Subnormals are mant * 2^-24 (the
+ * IEEE definition); the host decoder in [P1] scales them by 2^-14 instead,
+ * which is read here as a slip, since every normal value follows IEEE. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+/* f32 -> bf16 -> f32 with round-to-nearest-even on the 16 dropped bits.
+ * Used only by the diagnostic twin oracle_qmm_bf16. */
+float oracle_round_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7f800000u) == 0x7f800000u) { /* inf / nan unchanged */
+        return x;
+    }
+    uint32_t lower = u & 0xffffu;
+    uint32_t upper = u & 0xffff0000u;
+    uint32_t half = 0x8000u;
+    int odd = (u >> 16) & 1u;
+    if (lower > half || (lower == half && odd))
+        upper += 0x10000u; /* carry may roll into the exponent: correct */
+    float r;
+    memcpy(&r, &upper, 4);
+    return r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Row-parallel driver                                                      */
+/* ------------------------------------------------------------------------ */
+
+typedef void (*row_fn)(void *ctx, int64_t r0, int64_t r1);
+
+typedef struct {
+    row_fn fn;
+    void *ctx;
+    int64_t r0, r1;
+} row_task;
+
+static void *row_task_main(void *p)
+{
+    row_task *t = (row_task *)p;
+    t->fn(t->ctx, t->r0, t->r1);
+    return NULL;
+}
+
+/* Number of threads a call with `want` threads uses (want <= 0: all online
+ * cores), never more than the number of rows. */
+int oracle_threads(int want, int64_t rows)
+{
+    long n = want > 0 ? want : sysconf(_SC_NPROCESSORS_ONLN);
+    if (n < 1) n = 1;
+    if (n > 256) n = 256;
+    if (rows < n) n = rows > 0 ? (long)rows : 1;
+    return (int)n;
+}
+
+static int run_rows(row_fn fn, void *ctx, int64_t rows, int want)
+{
+    int n = oracle_threads(want, rows);
+    if (n == 1) {
+        fn(ctx, 0, rows);
+        return 1;
+    }
+    pthread_t th[256];
+    row_task tk[256];
+    for (int i = 0; i < n; ++i) {
+        tk[i].fn = fn;
+        tk[i].ctx = ctx;
+        tk[i].r0 = rows * i / n;
+        tk[i].r1 = rows * (i + 1) / n;
+        pthread_create(&th[i], NULL, row_task_main, &tk[i]);
+    }
+    for (int i = 0; i < n; ++i) pthread_join(th[i], NULL);
+    return n;
+}
+
+/* ------------------------------------------------------------------------ */
+/* q8_row matvec:  y[o] = rs[o] * sum_i q[o,i] * xs[i]          [P2] [P3]  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const int8_t *q;
+    const float *rs, *xs;
+    int64_t cols;
+    double *y, *mag;
+} q8_ctx;
+
+static void q8_rows(void *p, int64_t r0, int64_t r1)
+{
+    q8_ctx *c = (q8_ctx *)p;
+    for (int64_t o = r0; o < r1; ++o) {
+        const int8_t *row = c->q + o * c->cols;
+        double s = 0.0, a = 0.0;
+        for (int64_t i = 0; i < c->cols; ++i) {
+            double t = (double)row[i] * (double)c->xs[i];
+            s += t;
+            a += fabs(t);
+        }
+        c->y[o] = (double)c->rs[o] * s;
+        if (c->mag) c->mag[o] = fabs((double)c->rs[o]) * a;
+    }
+}
+
+/* q: [rows][cols] int8 row-major; rs: [rows]; xs: [cols].
+ * y[o] as defined above; mag[o] = |rs[o]| * sum_i |q[o,i]*xs[i]| (the
+ * magnitude the tolerances are stated against), may be NULL.
+ * Returns the number of threads used. */
+int oracle_q8row(const int8_t *q, const float *rs, const float *xs,
+                 int64_t rows, int64_t cols, double *y, double *mag,
+                 int nthreads)
+{
+    q8_ctx c = {q, rs, xs, cols, y, mag};
+    return run_rows(q8_rows, &c, rows, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batched q8_row product: y[b,o] = rs[o] * sum_i q[o,i] * xs[b,i]          */
+/* [P2] `q8_matmat` / [P3] `q8_matmat`: nb independent matvecs; output      */
+/* layout [nb][rows].                                                       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const int8_t *q;
+    const float *rs, *xs;
+    int64_t nb, rows, cols;
+    int round_bf16;
+    double *y, *mag;
+} qmm_ctx;
+
+static void qmm_rows(void *p, int64_t r0, int64_t r1)
+{
+    qmm_ctx *c = (qmm_ctx *)p;
+    for (int64_t o = r0; o < r1; ++o) {
+        const int8_t *row = c->q + o * c->cols;
+        for (int64_t b = 0; b < c->nb; ++b) {
+            const float *xb = c->xs + b * c->cols;
+            double s = 0.0, a = 0.0;
+            for (int64_t i = 0; i < c->cols; ++i) {
+                float xv = c->round_bf16 ? oracle_round_bf16(xb[i]) : xb[i];
+                double t = (double)row[i] * (double)xv;
+                s += t;
+                a += fabs(t);
+            }
+            c->y[b * c->rows + o] = (double)c->rs[o] * s;
+            if (c->mag) c->mag[b * c->rows + o] = fabs((double)c->rs[o]) * a;
+        }
+    }
+}
+
+int oracle_qmm(const int8_t *q, const float *rs, const float *xs, int64_t nb,
+               int64_t rows, int64_t cols, double *y, double *mag,
+               int nthreads)
+{
+    qmm_ctx c = {q, rs, xs, nb, rows, cols, 0, y, mag};
+    return run_rows(qmm_rows, &c, rows, nthreads);
+}
+
+/* Diagnostic twin: the same product with every xs value first rounded to
+ * bf16 (round to nearest even).  Not the contract; it tells indexing errors
+ * apart from the bf16 rounding the tensor-core path is allowed. */
+int oracle_qmm_bf16(const int8_t *q, const float *rs, const float *xs,
+                    int64_t nb, int64_t rows, int64_t cols, double *y,
+                    double *mag, int nthreads)
+{
+    qmm_ctx c = {q, rs, xs, nb, rows, cols, 1, y, mag};
+    return run_rows(qmm_rows, &c, rows, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* 2-bit group format ("Q2", g64 / g128)                                    */
+/*   q[m,k] = (codes[m][k/4] >> 2*(k%4)) & 3                                */
+/*   y[m]   = sum_g d[m,g] * sum_{k in group g} (q[m,k] - 1) * x[k]          */
+/* [P1] `dequant_embd` (bit order and d*(q-1)), block sizes in `upload_q2`. */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint8_t *codes;
+    const uint16_t *d;
+    const float *x;
+    int group;
+    int64_t cols;
+    double *y, *mag;
+} q2_ctx;
+
+static void q2_rows(void *p, int64_t r0, int64_t r1)
+{
+    q2_ctx *c = (q2_ctx *)p;
+    int64_t ngrp = c->cols / c->group;
+    int64_t row_bytes = c->cols / 4;
+    for (int64_t m = r0; m < r1; ++m) {
+        const uint8_t *row = c->codes + m * row_bytes;
+        double ym = 0.0, am = 0.0;
+        for (int64_t g = 0; g < ngrp; ++g) {
+            double dg = oracle_f16_to_f64(c->d[m * ngrp + g]);
+            double s = 0.0, a = 0.0;
+            for (int64_t kk = 0; kk < c->group; ++kk) {
+                int64_t k = g * c->group + kk;
+                int q = (row[k / 4] >> (2 * (k % 4))) & 3;
+                double t = (double)(q - 1) * (double)c->x[k];
+                s += t;
+                a += fabs(t);
+            }
+            ym += dg * s;
+            am += fabs(dg) * a;
+        }
+        c->y[m] = ym;
+        if (c->mag) c->mag[m] = am;
+    }
+}
+
+/* codes: [rows][cols/4] bytes; d: [rows][cols/group] f16 bit patterns;
+ * x: [cols]; group is 64 or 128 and divides cols.
+ * mag[m] = sum_g |d[m,g]| * sum_k |(q[m,k]-1) * x[k]|, may be NULL. */
+int oracle_q2(const uint8_t *codes, const uint16_t *d, int group,
+              const float *x, int64_t rows, int64_t cols, double *y,
+              double *mag, int nthreads)
+{
+    if (group != 64 && group != 128) return -1;
+    if (cols % group) return -1;
+    q2_ctx c = {codes, d, x, group, cols, y, mag};
+    return run_rows(q2_rows, &c, rows, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* MoE router select                     [P2] `moe_select_sg`, `moe_select` */
+/*  - softmax over all n logits: w_j = exp(l_j - max) / sum_all exp(l - max) */
+/*  - k rounds of argmax over the not-yet-chosen experts; equal values:     */
+/*    the lowest index wins (a strict '>' scan in index order)              */
+/*  - renorm != 0: divide the k selected weights by their sum               */
+/*  - shared expert pinned at slot k: sel[k] = n,                           */
+/*    w[k] = 1 / (1 + exp(-gate)), gate = sum_i sgw[i]*x[i] or *sg_logit     */
+/* Chosen experts are excluded by index, not by overwriting their logit    */
+/* with a sentinel, so any finite logit is handled.                         */
+/* ------------------------------------------------------------------------ */
+
+/* Returns the number of slots written (k, or k+1 with a shared expert), or
+ * -1 on bad arguments.  Logits must be finite. */
+int oracle_select(const float *logits, int n, int k, int renorm,
+                  const float *sgw, const float *x, int hidden,
+                  const float *sg_logit, int32_t *sel, double *w)
+{
+    if (n < 1 || k < 1 || k > n) return -1;
+    unsigned char *chosen = (unsigned char *)calloc((size_t)n, 1);
+    if (!chosen) return -1;
+    for (int s = 0; s < k; ++s) {
+        int best = -1;
+        for (int j = 0; j < n; ++j) {
+            if (chosen[j]) continue;
+            if (best < 0 || logits[j] > logits[best]) best = j;
+        }
+        chosen[best] = 1;
+        sel[s] = best;
+    }
+    free(chosen);
+
+    double mx = (double)logits[0];
+    for (int j = 1; j < n; ++j)
+        if ((double)logits[j] > mx) mx = (double)logits[j];
+    double den = 0.0;
+    for (int j = 0; j < n; ++j) den += exp((double)logits[j] - mx);
+    double wsum = 0.0;
+    for (int s = 0; s < k; ++s) {
+        w[s] = exp((double)logits[sel[s]] - mx) / den;
+        wsum += w[s];
+    }
+    if (renorm)
+        for (int s = 0; s < k; ++s) w[s] /= wsum;
+
+    if (!sgw && !sg_logit) return k; /* no shared expert */
+    double gate;
+    if (sgw) {
+        gate = 0.0;
+        for (int i = 0; i < hidden; ++i) gate += (double)sgw[i] * (double)x[i];
+    } else {
+        gate = (double)*sg_logit;
+    }
+    sel[k] = n;
+    w[k] = 1.0 / (1.0 + exp(-gate));
+    return k + 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* MoE expert FFN over the selected slots      [P2] `moe_gate_up`,          */
+/* `moe_down`; [P3] `moe_block`.                                            */
+/*  g_s = rs_g[e] . (Q_g[e] x),  u_s = rs_u[e] . (Q_u[e] x)   (per row r)    */
+/*  act_s[r] = silu(g_s[r]) * u_s[r],  silu(t) = t / (1 + exp(-t))          */
+/*  out[h] = sum_s w_s * rs_d[e][h] * sum_r Q_d[e][h,r] * act_s[r]           */
+/* with e = sel[s].  Expert stacks: gate/up [E][inter][hidden] int8 with    */
+/* rs [E][inter]; down [E][hidden][inter] int8 with rs [E][hidden].         */
+/* ------------------------------------------------------------------------ */
+
+/* Optional outputs (may be NULL): g, u, act as [slots][inter]; mag[h] =
+ * sum_s |w_s| * |rs_d[e][h]| * sum_r |Q_d[e][h,r] * act_s[r]|.
+ * Returns 0, or -1 if an expert index is out of range. */
+int oracle_moe_ffn(const int8_t *gq, const float *grs, const int8_t *uq,
+                   const float *urs, const int8_t *dq, const float *drs,
+                   int64_t n_experts, int64_t inter, int64_t hidden,
+                   const int32_t *sel, const double *w, int slots,
+                   const float *x, double *out, double *g_out,
+                   double *u_out, double *act_out, double *mag)
+{
+    double *act = (double *)malloc(sizeof(double) * (size_t)(slots * inter));
+    if (!act) return -1;
+    for (int s = 0; s < slots; ++s) {
+        if (sel[s] < 0 || sel[s] >= n_experts) {
+            free(act);
+            return -1;
+        }
+    }
+    for (int s = 0; s < slots; ++s) {
+        int64_t e = sel[s];
+        for (int64_t r = 0; r < inter; ++r) {
+            const int8_t *grow = gq + (e * inter + r) * hidden;
+            const int8_t *urow = uq + (e * inter + r) * hidden;
+            double sg = 0.0, su = 0.0;
+            for (int64_t i = 0; i < hidden; ++i) {
+                sg += (double)grow[i] * (double)x[i];
+                su += (double)urow[i] * (double)x[i];
+            }
+            double g = (double)grs[e * inter + r] * sg;
+            double u = (double)urs[e * inter + r] * su;
+            double a = g / (1.0 + exp(-g)) * u;
+            act[s * inter + r] = a;
+            if (g_out) g_out[s * inter + r] = g;
+            if (u_out) u_out[s * inter + r] = u;
+            if (act_out) act_out[s * inter + r] = a;
+        }
+    }
+    for (int64_t h = 0; h < hidden; ++h) {
+        double acc = 0.0, m = 0.0;
+        for (int s = 0; s < slots; ++s) {
+            int64_t e = sel[s];
+            const int8_t *drow = dq + (e * hidden + h) * inter;
+            double sd = 0.0, ad = 0.0;
+            for (int64_t r = 0; r < inter; ++r) {
+                double t = (double)drow[r] * act[s * inter + r];
+                sd += t;
+                ad += fabs(t);
+            }
+            double rsd = (double)drs[e * hidden + h];
+            acc += w[s] * rsd * sd;
+            m += fabs(w[s]) * fabs(rsd) * ad;
+        }
+        out[h] = acc;
+        if (mag) mag[h] = m;
+    }
+    free(act);
+    return 0;
+}

@@ -1,0 +1,43 @@
+"""Plants plausible mistakes in a copy of the oracle (on the CPU) and checks
+that the pins in test_oracle_pins.py catch every one of them."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTATIONS = [
+    ("q2_bit_order_reversed", "(row[k / 4] >> (2 * (k % 4))) & 3", "(row[k / 4] >> (2 * (3 - k % 4))) & 3"),
+    ("q2_offset_dropped", "(double)(q - 1) * (double)c->x[k]", "(double)(q) * (double)c->x[k]"),
+    ("q2_wrong_group_scale", "c->d[m * ngrp + g]", "c->d[m * ngrp]"),
+    ("f16_subnormal_scale", "ldexp((double)m, -24)", "ldexp((double)m, -14)"),
+    ("q8_row_scale_dropped", "c->y[o] = (double)c->rs[o] * s;", "c->y[o] = s;"),
+    ("qmm_transposed_output", "c->y[b * c->rows + o] = (double)c->rs[o] * s;", "c->y[o * c->nb + b] = (double)c->rs[o] * s;"),
+    ("select_tie_highest_index", "logits[j] > logits[best]", "logits[j] >= logits[best]"),
+    ("select_no_renorm", "if (renorm)\n        for (int s = 0; s < k; ++s) w[s] /= wsum;", ""),
+    ("select_denominator_selected_only", "for (int j = 0; j < n; ++j) den += exp((double)logits[j] - mx);",
+     "for (int j = 0; j < k; ++j) den += exp((double)logits[sel[j]] - mx);"),
+    ("moe_silu_sign", "double a = g / (1.0 + exp(-g)) * u;", "double a = g / (1.0 + exp(g)) * u;"),
+    ("moe_weight_dropped", "acc += w[s] * rsd * sd;", "acc += rsd * sd;"),
+    ("bf16_round_truncates", "if (lower > half || (lower == half && odd))", "if (0)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "oracle_mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-pthread", str(mut), "-o", str(lib), "-lm"])
+    env = dict(os.environ, QMV_ORACLE_LIB_OVERRIDE=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutation {name} survived the pins:\n{r.stdout[-2000:]}"

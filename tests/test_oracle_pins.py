@@ -1,0 +1,364 @@
+"""Pins for the fp64 oracle: each test fixes the oracle against something other
+than itself -- hand-worked examples (tests/golden/), closed forms, exact
+integer arithmetic, unit-vector probes, a separately written
+dequantise-then-dense product, the g128 = two-g64 identity and brute-force
+top-k.  No GPU; nothing here touches the CUDA library."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_decode_prefill_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _fixture(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = v.strip()
+    return out
+
+
+def _nums(s, dtype=float):
+    return [dtype(t) for t in s.split()]
+
+
+# ----------------------------------------------------------------- goldens
+
+def test_golden_q8row():
+    g = _fixture("q8row_worked.txt")
+    rows, cols = int(g["rows"]), int(g["cols"])
+    q = np.array(_nums(g["q"], int), np.int8).reshape(rows, cols)
+    y = oracle.q8row(q, _nums(g["rs"]), _nums(g["xs"]))
+    assert y.tolist() == _nums(g["y"])
+
+
+def _q2_fixture(name):
+    g = _fixture(name)
+    group, rows, cols = int(g["group"]), int(g["rows"]), int(g["cols"])
+    codes = np.frombuffer(bytes.fromhex(g["codes_hex"]), np.uint8).reshape(rows, cols // 4)
+    d = np.array([int(g["d_hex"], 16)], np.uint16).reshape(rows, cols // group)
+    xs = g["x"].split()
+    if xs == ["ones"]:
+        x = np.ones(cols, np.float32)
+    else:
+        head = [float(t) for t in xs if not t.startswith("fill")]
+        fill = float(xs[-1][4:]) if xs[-1].startswith("fill") else 0.0
+        x = np.full(cols, fill, np.float32)
+        x[:len(head)] = head
+    return group, codes, d, x, _nums(g["y"])
+
+
+@pytest.mark.parametrize("name", ["q2_g64_worked.txt", "q2_g128_worked.txt",
+                                  "q2_bitorder_worked.txt"])
+def test_golden_q2(name):
+    group, codes, d, x, y_ref = _q2_fixture(name)
+    y = oracle.q2(codes, d, group, x)
+    assert y.tolist() == y_ref
+
+
+def test_golden_select():
+    g = _fixture("select_worked.txt")
+    logits = np.array(_nums(g["logits"]), np.float32)
+    k = int(g["top_k"])
+    for renorm, key in ((False, "w_plain"), (True, "w_renorm")):
+        sel, w = oracle.select(logits, k, renorm, sg_logit=float(g["sg_logit"]))
+        assert sel.tolist() == _nums(g["sel"], int)
+        np.testing.assert_allclose(w, _nums(g[key]), rtol=1e-15, atol=0)
+
+
+# ------------------------------------------------------- scalar decoders
+
+def test_f16_decode_matches_ieee_library():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # a subnormal: mant * 2^-24
+    assert oracle.f16_to_f64(0x0001) == 2.0 ** -24
+
+
+def test_bf16_round_matches_torch():
+    g = synth.rng(11)
+    x = g.standard_normal(20000).astype(np.float32)
+    # exact ties and near-ties around the rounding point
+    base = x.view(np.uint32) & np.uint32(0xFFFF0000)
+    ties = (base | np.uint32(0x8000)).view(np.float32)
+    near = (base | np.uint32(0x7FFF)).view(np.float32)
+    allx = np.concatenate([x, ties, near, np.float32([0.0, -0.0, 3.4e38, -3.4e38, 1e-40])])
+    ref = torch.from_numpy(allx).to(torch.bfloat16).to(torch.float32).numpy()
+    got = np.array([oracle.round_bf16(v) for v in allx], np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------------ q8_row
+
+def test_q8_unit_vector_probe():
+    q, rs, _ = synth.q8_inputs(37, 48, seed=5)
+    for j in (0, 1, 17, 47):
+        x = np.zeros(48, np.float32); x[j] = 1.0
+        y = oracle.q8row(q, rs, x)
+        assert np.array_equal(y, rs.astype(np.float64) * q[:, j].astype(np.float64))
+
+
+def test_q8_exact_integer_arithmetic():
+    g = synth.rng(6)
+    q = g.integers(-128, 128, size=(23, 64), dtype=np.int8)
+    xs = g.integers(-2, 3, size=64).astype(np.float32)
+    rs = (2.0 ** g.integers(-8, 3, size=23)).astype(np.float32)
+    y = oracle.q8row(q, rs, xs)
+    for o in range(23):
+        s = sum(int(q[o, i]) * int(xs[i]) for i in range(64))
+        assert y[o] == float(rs[o]) * s
+
+
+def test_q8_matches_dense_fp64_matmul():
+    q, rs, xs = synth.q8_inputs(300, 512, seed=7)
+    y, mag = oracle.q8row(q, rs, xs, with_mag=True)
+    qd = q.astype(np.float64)
+    ref = rs.astype(np.float64) * (qd @ xs.astype(np.float64))
+    refmag = np.abs(rs.astype(np.float64)) * (np.abs(qd) @ np.abs(xs.astype(np.float64)))
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12 * refmag.max())
+    np.testing.assert_allclose(mag, refmag, rtol=1e-12)
+
+
+def test_q8_threads_do_not_change_results():
+    q, rs, xs = synth.q8_inputs(257, 256, seed=8)
+    y1 = oracle.q8row(q, rs, xs, nthreads=1)
+    y7 = oracle.q8row(q, rs, xs, nthreads=7)
+    assert np.array_equal(y1, y7)
+
+
+# -------------------------------------------------------------------- qmm
+
+def test_qmm_rows_are_independent_matvecs():
+    q, rs, xs = synth.qmm_inputs(40, 96, 5, seed=9)
+    y = oracle.qmm(q, rs, xs)
+    assert y.shape == (5, 40)
+    for b in range(5):
+        assert np.array_equal(y[b], oracle.q8row(q, rs, xs[b]))
+
+
+def test_qmm_nb1_equals_q8row():
+    q, rs, xs = synth.qmm_inputs(33, 64, 1, seed=10)
+    assert np.array_equal(oracle.qmm(q, rs, xs)[0], oracle.q8row(q, rs, xs[0]))
+
+
+def test_qmm_bf16_twin_is_qmm_on_rounded_xs():
+    q, rs, xs = synth.qmm_inputs(31, 80, 3, seed=12)
+    xr = torch.from_numpy(xs).to(torch.bfloat16).to(torch.float32).numpy()
+    assert np.array_equal(oracle.qmm(q, rs, xs, bf16_xs=True), oracle.qmm(q, rs, xr))
+    assert not np.array_equal(xr, xs)
+
+
+# --------------------------------------------------------------------- Q2
+
+def _pack_codes(cmat):
+    """Test-local packer: code k of a row -> byte k/4, bits 2(k%4)."""
+    rows, cols = cmat.shape
+    out = np.zeros((rows, cols // 4), np.uint8)
+    for b in range(4):
+        out |= (cmat[:, b::4].astype(np.uint8) << (2 * b))
+    return out
+
+
+def _dequant_dense(codes, d_bits, group):
+    """Separately written dequantiser: dense fp64 W from codes and f16 d."""
+    rows = codes.shape[0]
+    cols = codes.shape[1] * 4
+    bits = np.unpackbits(codes[:, :, None], axis=2, bitorder="little")  # [r][c/4][8]
+    q = (bits[:, :, 0::2] + 2 * bits[:, :, 1::2]).reshape(rows, cols).astype(np.float64)
+    d = d_bits.view(np.float16).astype(np.float64)
+    return np.repeat(d, group, axis=1) * (q - 1.0)
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_unit_vector_probe_bit_order(group):
+    g = synth.rng(13)
+    rows, cols = 9, 2 * group
+    cmat = g.integers(0, 4, size=(rows, cols))
+    codes = _pack_codes(cmat)
+    d_bits = g.uniform(0.01, 1.0, size=(rows, cols // group)).astype(np.float16).view(np.uint16)
+    dd = d_bits.view(np.float16).astype(np.float64)
+    for j in range(cols):
+        x = np.zeros(cols, np.float32); x[j] = 1.0
+        y = oracle.q2(codes, d_bits, group, x)
+        assert np.array_equal(y, dd[:, j // group] * (cmat[:, j] - 1.0)), j
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_matches_dequantise_then_dense(group):
+    codes, d_bits, x = synth.q2_inputs(200, 1024, group, seed=14)
+    y, mag = oracle.q2(codes, d_bits, group, x, with_mag=True)
+    W = _dequant_dense(codes, d_bits, group)
+    ref = W @ x.astype(np.float64)
+    refmag = np.abs(W) @ np.abs(x.astype(np.float64))
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12 * refmag.max())
+    np.testing.assert_allclose(mag, refmag, rtol=1e-12)
+
+
+def test_q2_g128_equals_two_g64_sharing_d():
+    codes, d128, x = synth.q2_inputs(64, 1024, 128, seed=15)
+    # one g128 block == two g64 blocks with the same d (codes unchanged)
+    d64 = np.repeat(d128, 2, axis=1)
+    y128 = oracle.q2(codes, d128, 128, x)
+    y64 = oracle.q2(codes, d64, 64, x)
+    np.testing.assert_allclose(y128, y64, rtol=1e-13, atol=1e-13)
+
+
+def test_q2_exact_integer_arithmetic():
+    g = synth.rng(16)
+    rows, cols, group = 11, 256, 64
+    cmat = g.integers(0, 4, size=(rows, cols))
+    codes = _pack_codes(cmat)
+    dexp = g.integers(-4, 2, size=(rows, cols // group))
+    d_bits = (2.0 ** dexp).astype(np.float16).view(np.uint16)
+    x = g.integers(-3, 4, size=cols).astype(np.float32)
+    y = oracle.q2(codes, d_bits, group, x)
+    for m in range(rows):
+        tot = 0.0
+        for gi in range(cols // group):
+            s = sum((int(cmat[m, k]) - 1) * int(x[k])
+                    for k in range(gi * group, (gi + 1) * group))
+            tot += (2.0 ** int(dexp[m, gi])) * s
+        assert y[m] == tot
+
+
+def test_q2_rejects_bad_group():
+    codes, d, x = synth.q2_inputs(2, 128, 64, seed=17)
+    with pytest.raises(ValueError):
+        oracle.q2(codes, d, 32, x)
+
+
+# ---------------------------------------------------------------- select
+
+def _brute_topk(logits, k):
+    """Exhaustive: the unique k-subset whose every member beats every
+    non-member (greater value, or equal value and lower index), listed by
+    (value desc, index asc)."""
+    n = len(logits)
+
+    def beats(i, j):
+        return logits[i] > logits[j] or (logits[i] == logits[j] and i < j)
+
+    winners = []
+    for subset in itertools.combinations(range(n), k):
+        rest = [j for j in range(n) if j not in subset]
+        if all(beats(i, j) for i in subset for j in rest):
+            winners.append(subset)
+    assert len(winners) == 1
+    return sorted(winners[0], key=lambda i: (-logits[i], i))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
+def test_select_bruteforce(n):
+    g = synth.rng(100 + n)
+    cases = [g.standard_normal(n).astype(np.float32),
+             g.integers(0, 3, size=n).astype(np.float32),     # tie-heavy
+             np.zeros(n, np.float32),
+             np.array([(-1) ** i * 0.0 for i in range(n)], np.float32)]  # +0 / -0
+    for logits in cases:
+        for k in range(1, n + 1):
+            sel, _ = oracle.select(logits, k, False)
+            assert sel.tolist() == _brute_topk(logits.tolist(), k)
+
+
+def test_select_softmax_closed_forms():
+    n = 12
+    sel, w = oracle.select(np.full(n, 0.7, np.float32), 5, False)
+    assert sel.tolist() == [0, 1, 2, 3, 4]
+    np.testing.assert_allclose(w, 1.0 / n, rtol=1e-15)
+    _, w = oracle.select(np.full(n, 0.7, np.float32), 5, True)
+    np.testing.assert_allclose(w, 1.0 / 5, rtol=1e-15)
+    # two-level logits: a ones and (n-a) zeros
+    a = 3
+    lg = np.array([1.0] * a + [0.0] * (n - a), np.float32)
+    _, w = oracle.select(lg, a + 2, False)
+    den = a + (n - a) * math.exp(-1.0)
+    np.testing.assert_allclose(w[:a], 1.0 / den, rtol=1e-15)
+    np.testing.assert_allclose(w[a:], math.exp(-1.0) / den, rtol=1e-15)
+
+
+def test_select_shared_gate():
+    g = synth.rng(18)
+    sgw = g.standard_normal(64).astype(np.float32)
+    x = g.standard_normal(64).astype(np.float32)
+    logits = g.standard_normal(16).astype(np.float32)
+    sel, w = oracle.select(logits, 4, True, sgw=sgw, x=x)
+    gate = math.fsum(float(a) * float(b) for a, b in zip(sgw, x))
+    assert sel[-1] == 16 and len(sel) == 5
+    assert abs(w[-1] - 1.0 / (1.0 + math.exp(-gate))) < 1e-15
+    np.testing.assert_allclose(w[:4].sum(), 1.0, rtol=1e-15)
+    # no shared expert -> top_k slots only
+    sel2, _ = oracle.select(logits, 4, True)
+    assert len(sel2) == 4 and sel2.tolist() == sel[:4].tolist()
+
+
+# ------------------------------------------------------------------- MoE
+
+def _moe_dense(m, sel, w):
+    x = m.x.astype(np.float64)
+    out = np.zeros(m.dq.shape[1])
+    for s, e in enumerate(sel):
+        g = m.grs[e].astype(np.float64) * (m.gq[e].astype(np.float64) @ x)
+        u = m.urs[e].astype(np.float64) * (m.uq[e].astype(np.float64) @ x)
+        act = g / (1.0 + np.exp(-g)) * u
+        out += w[s] * m.drs[e].astype(np.float64) * (m.dq[e].astype(np.float64) @ act)
+    return out
+
+
+def test_moe_single_expert_reduces_to_one_ffn():
+    m = synth.moe_inputs(n_exp=6, hidden=64, inter=48, seed=19)
+    sel, w = oracle.select(m.logits, 1, True, sg_logit=-1e4)
+    assert w[0] == 1.0 and w[1] == 0.0
+    out = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel, w, m.x)
+    e = int(sel[0])
+    ref = _moe_dense(m, [e], [1.0])
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+
+
+def test_moe_matches_dense_formula():
+    m = synth.moe_inputs(n_exp=10, hidden=96, inter=64, seed=20)
+    sel, w = oracle.select(m.logits, 3, True, sgw=m.sgw, x=m.x)
+    out, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel, w, m.x,
+                                with_parts=True)
+    ref = _moe_dense(m, sel.tolist(), w.tolist())
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    # act = silu(g) * u with the oracle's own g, u
+    g, u = parts["g"], parts["u"]
+    np.testing.assert_allclose(parts["act"], g / (1 + np.exp(-g)) * u, rtol=1e-14)
+
+
+def test_moe_rejects_bad_expert():
+    m = synth.moe_inputs(n_exp=3, hidden=32, inter=16, seed=21)
+    with pytest.raises(ValueError):
+        oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs,
+                       np.array([5], np.int32), np.array([1.0]), m.x)
+
+
+# --------------------------------------------------------------- synth
+
+def test_synth_is_deterministic_and_in_range():
+    a = synth.q8_inputs(64, 128, seed=0)
+    b = synth.q8_inputs(64, 128, seed=0)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+    q, rs, xs = a
+    assert q.min() >= -127 and q.max() <= 127
+    assert rs.min() >= 1e-3 and rs.max() <= 1e-2
+    codes, d, x = synth.q2_inputs(16, 256, 64, seed=1)
+    dv = d.view(np.float16).astype(np.float32)
+    assert dv.min() >= 0.0049 and dv.max() <= 0.0501
+    assert codes.shape == (16, 64) and d.shape == (16, 4)
