@@ -1,0 +1,353 @@
+// libqmv: status/error plumbing, the load-time repack and handle lifetime.
+//
+// The repack is the load-time reorder the pages do once at upload
+// (qxmx_gpu.cpp, `upload_q2` with `repack_q2_g64` / `repack_q2_g128`): the
+// weights are rearranged so that the decode kernels read each weight byte
+// exactly once, in 512-byte coalesced warp transactions, in the order their
+// arithmetic consumes it.  Layouts are described in qmv_internal.cuh.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "qmv_internal.cuh"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+thread_local int g_msg_status = 0;
+
+__device__ int g_dev_status;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int* status = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceState g_devs[kMaxDevices];
+std::mutex g_devs_mu;
+
+DeviceState* device_state() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_devs_mu);
+    DeviceState& s = g_devs[dev];
+    if (!s.ready) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dev_status) != cudaSuccess) return nullptr;
+        s.sms = sms;
+        s.status = static_cast<int*>(p);
+        s.ready = true;
+    }
+    return &s;
+}
+
+}  // namespace
+
+namespace qmv {
+
+qmv_status fail(qmv_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    g_msg_status = st;
+    return st;
+}
+
+qmv_status check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(QMV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return QMV_OK;
+}
+
+int sm_count() {
+    DeviceState* s = device_state();
+    return s ? s->sms : 148;
+}
+
+int* device_status() {
+    DeviceState* s = device_state();
+    return s ? s->status : nullptr;
+}
+
+int current_device() {
+    int d = -1;
+    cudaGetDevice(&d);
+    return d;
+}
+
+}  // namespace qmv
+
+// ---------------------------------------------------------------------------
+// Repack kernels (integer byte moves only).
+// ---------------------------------------------------------------------------
+
+// One thread per 16-byte lane chunk (row group, 128-column block, lane) of
+// one expert: gathers 4 rows x 4 columns from the row-major source.
+__global__ void pack_q8row_kernel(const int8_t* __restrict__ src, const float* __restrict__ rs_src,
+                                  int8_t* __restrict__ dst, float* __restrict__ rs_dst,
+                                  int64_t experts, int64_t rows, int64_t cols,
+                                  int64_t rows_pad, int64_t cols_pad) {
+    const int64_t nblk = cols_pad / 128;
+    const int64_t per_expert = (rows_pad / 4) * nblk * 32;
+    const int64_t total = experts * per_expert;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = i / per_expert;
+        int64_t r = i % per_expert;
+        const int lane = (int)(r % 32);
+        r /= 32;
+        const int64_t blk = r % nblk;
+        const int64_t rg = r / nblk;
+        const int64_t col0 = blk * 128 + lane * 4;
+        uint32_t words[4];
+        for (int rr = 0; rr < 4; ++rr) {
+            const int64_t row = rg * 4 + rr;
+            uint32_t w = 0;
+            if (row < rows && col0 < cols) {
+                // cols % 16 == 0 and col0 % 4 == 0: the 4 bytes are aligned and in range
+                w = *reinterpret_cast<const uint32_t*>(src + (e * rows + row) * cols + col0);
+            }
+            words[rr] = w;
+        }
+        uint4 v = make_uint4(words[0], words[1], words[2], words[3]);
+        *reinterpret_cast<uint4*>(dst + e * rows_pad * cols_pad + rg * 4 * cols_pad + blk * 512 + lane * 16) = v;
+    }
+    const int64_t nrs = experts * rows_pad;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nrs;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = i / rows_pad, row = i % rows_pad;
+        rs_dst[i] = row < rows ? rs_src[e * rows + row] : 0.0f;
+    }
+}
+
+// One thread per packed 32-bit code word (row tile, column chunk, lane, word).
+__global__ void pack_q2_codes_kernel(const uint8_t* __restrict__ src, uint32_t* __restrict__ dst,
+                                     int64_t rows, int64_t cols, int64_t rt_count, int64_t kc_count) {
+    const int64_t total = rt_count * kc_count * 32 * 4;
+    const int64_t row_bytes = cols / 4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(i % 4);
+        const int lane = (int)((i / 4) % 32);
+        const int64_t kc = (i / 128) % kc_count;
+        const int64_t rt = i / (128 * kc_count);
+        uint32_t w = 0;
+        for (int t = 0; t < 8; ++t) {
+            const int s = 2 * j + t / 4;
+            const int fr = t % 4;
+            const int64_t row = rt * 16 + lane / 4 + 8 * (fr & 1);
+            for (int h = 0; h < 2; ++h) {
+                const int64_t col = kc * 128 + 16 * s + 2 * (lane % 4) + 8 * (fr >> 1) + h;
+                uint32_t code = 1;  // padding: code 1 is the weight 0
+                if (row < rows && col < cols) code = (src[row * row_bytes + col / 4] >> (2 * (col % 4))) & 3u;
+                w |= code << (2 * t + 16 * h);
+            }
+        }
+        dst[i] = w;
+    }
+}
+
+// One thread per packed scale (row tile, chunk, l/4, row half, group in chunk).
+__global__ void pack_q2_scales_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                      int64_t rows, int64_t cols, int group, int64_t rt_count,
+                                      int64_t kc_count) {
+    const int gpc = 128 / group;
+    const int64_t ngrp = cols / group;
+    const int64_t total = rt_count * kc_count * 16 * gpc;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int gi = (int)(i % gpc);
+        const int rhi = (int)((i / gpc) % 2);
+        const int r0 = (int)((i / (2 * gpc)) % 8);
+        const int64_t kc = (i / (16 * gpc)) % kc_count;
+        const int64_t rt = i / (16 * gpc * kc_count);
+        const int64_t row = rt * 16 + r0 + 8 * rhi;
+        const int64_t g = kc * gpc + gi;
+        dst[i] = (row < rows && g < ngrp) ? src[row * ngrp + g] : (uint16_t)0;
+    }
+}
+
+namespace {
+
+int grid_for(int64_t n, int threads) {
+    int64_t b = (n + threads - 1) / threads;
+    int64_t cap = (int64_t)qmv::sm_count() * 16;
+    if (b > cap) b = cap;
+    if (b < 1) b = 1;
+    return (int)b;
+}
+
+qmv_status alloc_handle(qmv_weights** out, int64_t bytes) {
+    qmv_weights* w = new (std::nothrow) qmv_weights();
+    if (!w) return qmv::fail(QMV_ERR_ALLOC, "host allocation of the handle failed");
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, (size_t)bytes);
+    if (e != cudaSuccess) {
+        delete w;
+        cudaGetLastError();
+        return qmv::fail(QMV_ERR_ALLOC, "cudaMalloc(%lld bytes) for packed weights failed: %s",
+                         (long long)bytes, cudaGetErrorString(e));
+    }
+    w->base = p;
+    w->bytes = bytes;
+    w->device = qmv::current_device();
+    *out = w;
+    return QMV_OK;
+}
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+extern "C" {
+
+const char* qmv_status_string(int status) {
+    switch (status) {
+        case QMV_OK: return "QMV_OK";
+        case QMV_ERR_INVALID_ARG: return "QMV_ERR_INVALID_ARG";
+        case QMV_ERR_UNSUPPORTED: return "QMV_ERR_UNSUPPORTED";
+        case QMV_ERR_ALLOC: return "QMV_ERR_ALLOC";
+        case QMV_ERR_CUDA: return "QMV_ERR_CUDA";
+        case QMV_ERR_DEVICE_STATUS: return "QMV_ERR_DEVICE_STATUS";
+        default: return "QMV_ERR_UNKNOWN";
+    }
+}
+
+int qmv_last_error(char* buf, size_t n) {
+    if (buf && n > 0) {
+        strncpy(buf, g_msg, n - 1);
+        buf[n - 1] = '\0';
+    }
+    return g_msg_status;
+}
+
+int qmv_version(void) { return 100; }
+
+qmv_status qmv_pack_q8row(const int8_t* q, const float* rs, int64_t experts, int64_t rows,
+                          int64_t cols, qmv_stream st, qmv_weights** out) {
+    QMV_REQUIRE(out, QMV_ERR_INVALID_ARG, "qmv_pack_q8row: out is NULL");
+    *out = nullptr;
+    QMV_REQUIRE(q && rs, QMV_ERR_INVALID_ARG, "qmv_pack_q8row: q or rs is NULL");
+    QMV_REQUIRE(experts >= 1 && rows >= 1, QMV_ERR_INVALID_ARG, "qmv_pack_q8row: experts and rows must be >= 1");
+    QMV_REQUIRE(cols >= 16 && cols % 16 == 0, QMV_ERR_INVALID_ARG,
+                "qmv_pack_q8row: cols must be a positive multiple of 16 (got %lld)", (long long)cols);
+    QMV_REQUIRE(qmv::aligned16(q), QMV_ERR_INVALID_ARG, "qmv_pack_q8row: q must be 16-byte aligned");
+    QMV_REQUIRE(rows <= (int64_t)1 << 31 && cols <= (int64_t)1 << 24, QMV_ERR_UNSUPPORTED,
+                "qmv_pack_q8row: matrix too large");
+    const int64_t rows_pad = round_up(rows, kQ8RowPad);
+    const int64_t cols_pad = round_up(cols, 128);
+    const int64_t qbytes = experts * rows_pad * cols_pad;
+    const int64_t rsbytes = experts * rows_pad * 4;
+    qmv_weights* w = nullptr;
+    qmv_status s = alloc_handle(&w, qbytes + round_up(rsbytes, 256));
+    if (s != QMV_OK) return s;
+    w->format = QMV_FMT_Q8ROW;
+    w->group = 0;
+    w->experts = experts;
+    w->rows = rows;
+    w->cols = cols;
+    w->rows_pad = rows_pad;
+    w->cols_pad = cols_pad;
+    w->q = static_cast<int8_t*>(w->base);
+    w->rs = reinterpret_cast<float*>(static_cast<char*>(w->base) + qbytes);
+    const int64_t n = experts * (rows_pad / 4) * (cols_pad / 128) * 32;
+    pack_q8row_kernel<<<grid_for(n, 256), 256, 0, (cudaStream_t)st>>>(q, rs, w->q, w->rs, experts, rows,
+                                                                      cols, rows_pad, cols_pad);
+    s = qmv::check_launch("pack_q8row_kernel");
+    if (s != QMV_OK) {
+        cudaFree(w->base);
+        delete w;
+        return s;
+    }
+    *out = w;
+    return QMV_OK;
+}
+
+qmv_status qmv_pack_q2(const uint8_t* codes, const uint16_t* d, int group, int64_t rows,
+                       int64_t cols, qmv_stream st, qmv_weights** out) {
+    QMV_REQUIRE(out, QMV_ERR_INVALID_ARG, "qmv_pack_q2: out is NULL");
+    *out = nullptr;
+    QMV_REQUIRE(codes && d, QMV_ERR_INVALID_ARG, "qmv_pack_q2: codes or d is NULL");
+    QMV_REQUIRE(group == 64 || group == 128, QMV_ERR_INVALID_ARG, "qmv_pack_q2: group must be 64 or 128 (got %d)", group);
+    QMV_REQUIRE(rows >= 1 && cols >= group && cols % group == 0, QMV_ERR_INVALID_ARG,
+                "qmv_pack_q2: need rows >= 1 and cols a positive multiple of the group (rows=%lld cols=%lld)",
+                (long long)rows, (long long)cols);
+    QMV_REQUIRE(rows <= (int64_t)1 << 30 && cols <= 32768, QMV_ERR_UNSUPPORTED,
+                "qmv_pack_q2: supports cols <= 32768 (got %lld)", (long long)cols);
+    const int64_t rows_pad = round_up(rows, kQ2RowPad);
+    const int64_t cols_pad = round_up(cols, 128);
+    const int64_t rt = rows_pad / 16, kc = cols_pad / 128;
+    const int64_t cbytes = rt * kc * 512;
+    const int64_t dbytes = rt * kc * 16 * (128 / group) * 2;
+    qmv_weights* w = nullptr;
+    qmv_status s = alloc_handle(&w, cbytes + round_up(dbytes, 256));
+    if (s != QMV_OK) return s;
+    w->format = group == 64 ? QMV_FMT_Q2G64 : QMV_FMT_Q2G128;
+    w->group = group;
+    w->experts = 1;
+    w->rows = rows;
+    w->cols = cols;
+    w->rows_pad = rows_pad;
+    w->cols_pad = cols_pad;
+    w->codes = static_cast<uint4*>(w->base);
+    w->d = reinterpret_cast<__half*>(static_cast<char*>(w->base) + cbytes);
+    cudaStream_t cs = (cudaStream_t)st;
+    pack_q2_codes_kernel<<<grid_for(rt * kc * 128, 256), 256, 0, cs>>>(
+        codes, reinterpret_cast<uint32_t*>(w->codes), rows, cols, rt, kc);
+    pack_q2_scales_kernel<<<grid_for(rt * kc * 16 * (128 / group), 256), 256, 0, cs>>>(
+        d, reinterpret_cast<uint16_t*>(w->d), rows, cols, group, rt, kc);
+    s = qmv::check_launch("pack_q2 kernels");
+    if (s != QMV_OK) {
+        cudaFree(w->base);
+        delete w;
+        return s;
+    }
+    *out = w;
+    return QMV_OK;
+}
+
+qmv_status qmv_weights_info(const qmv_weights* w, int* format, int64_t* experts, int64_t* rows,
+                            int64_t* cols, int64_t* device_bytes) {
+    QMV_REQUIRE(w, QMV_ERR_INVALID_ARG, "qmv_weights_info: handle is NULL");
+    if (format) *format = w->format;
+    if (experts) *experts = w->experts;
+    if (rows) *rows = w->rows;
+    if (cols) *cols = w->cols;
+    if (device_bytes) *device_bytes = w->bytes;
+    return QMV_OK;
+}
+
+qmv_status qmv_weights_free(qmv_weights* w) {
+    if (!w) return QMV_OK;
+    int prev = qmv::current_device();
+    if (prev != w->device) cudaSetDevice(w->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t f = cudaFree(w->base);
+    if (prev != w->device && prev >= 0) cudaSetDevice(prev);
+    delete w;
+    if (e != cudaSuccess || f != cudaSuccess)
+        return qmv::fail(QMV_ERR_CUDA, "qmv_weights_free: %s",
+                         cudaGetErrorString(e != cudaSuccess ? e : f));
+    return QMV_OK;
+}
+
+qmv_status qmv_check(qmv_stream st, int* code) {
+    int* p = qmv::device_status();
+    QMV_REQUIRE(p, QMV_ERR_CUDA, "qmv_check: no CUDA device");
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)st);
+    if (e == cudaSuccess && v != 0) e = cudaMemsetAsync(p, 0, sizeof(int), (cudaStream_t)st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)st);
+    if (e != cudaSuccess) return qmv::fail(QMV_ERR_CUDA, "qmv_check: %s", cudaGetErrorString(e));
+    if (code) *code = v;
+    if (v != 0) return qmv::fail(QMV_ERR_DEVICE_STATUS, "qmv_check: device status %d", v);
+    return QMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,437 @@
+// Prefill GEMM for q8_row weights on the 5th-generation tensor cores:
+//   y[b,o] = rs[o] * sum_i q[o,i] * xs[b,i]
+//
+// Prior art: cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `q8_mul_mm`
+// (register-blocked fp32 tiles, rs applied at the store) and cortiq-engine
+// 0.3.7 src/gpu_metal.rs, MSL `q8_mul_mm` (8x8 simdgroup-matrix tiles with
+// rs folded into a half W tile).  Here rs stays out of the operands: the
+// int8 codes become bf16 exactly, xs is rounded once to bf16 (nearest
+// even), the products accumulate in fp32 in tensor memory, and rs multiplies
+// the fp32 result in the epilogue.
+//
+// Structure (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: the int8 W tile (a 4-D tensor map over the
+//               packed row-group layout) and the bf16 xs tile (128-byte
+//               swizzle), both into a 4-stage shared-memory ring;
+//   warp 1      TMEM allocator and the single thread that issues
+//               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32);
+//   warps 4-7   dequant: int8 -> bf16 into the canonical K-major
+//               128-byte-swizzled operand layout;
+//   warps 8-11  epilogue: tcgen05.ld from TMEM (double-buffered
+//               accumulators, 2 x 256 columns), x rs[o], coalesced stores.
+// Every mbarrier wait is bounded; on expiry the kernel records
+// kDevTimeout in the device status word and drains instead of hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qmv_internal.cuh"
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int kA8Bytes = BM * BK;        // int8 A tile
+constexpr int kABytes = BM * BK * 2;     // bf16 A tile
+constexpr int kBBytes = BN * BK * 2;     // bf16 B tile
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;           // two 256-column accumulators
+constexpr uint32_t kSpinFast = 4096;
+constexpr uint32_t kSpinLimit = 1u << 22;  // ~1 s with the backoff below
+
+struct __align__(1024) Smem {
+    uint8_t b[STAGES][kBBytes];
+    uint8_t a[STAGES][kABytes];
+    uint8_t a8[STAGES][kA8Bytes];
+    uint64_t full[STAGES];
+    uint64_t aready[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with parity `parity`.  Returns false if the
+// kernel is aborting (this wait expired, or another role's did).
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort, int* status) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (mbar_try(b, parity)) return true;
+        if (i >= kSpinFast) {
+            if (*abort) return false;
+            __nanosleep(256);
+        }
+    }
+    *abort = 1;
+    atomicCAS(status, 0, qmv::kDevTimeout);
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, "
+        "%6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                     // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset
+    d |= (uint64_t)1 << 46;                     // descriptor version
+    d |= (uint64_t)2 << 61;                     // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%"
+        "18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]),
+          "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]),
+          "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Exact int8 -> bf16 for the 4 bytes of a word (two bf16x2 results).
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+    const float2 f01 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))),
+                                  bias);
+    const float2 f23 = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                              __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))),
+                                  bias);
+    const __nv_bfloat162 b01 = __float22bfloat162_rn(f01);
+    const __nv_bfloat162 b23 = __float22bfloat162_rn(f23);
+    lo = *reinterpret_cast<const uint32_t*>(&b01);
+    hi = *reinterpret_cast<const uint32_t*>(&b23);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                                  const __grid_constant__ CUtensorMap tmB,
+                                                                  const float* __restrict__ rs,
+                                                                  float* __restrict__ y, int rows, int nb,
+                                                                  int ksteps, int m_tiles, int n_tiles,
+                                                                  int* __restrict__ status) {
+    extern __shared__ uint8_t smem_raw[];
+    Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    volatile int* abort = &sm.abort;
+    const int num_tiles = m_tiles * n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.aready[s], 4);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&sm.tfull[a], 1);
+            mbar_init(&sm.tempty[a], 4);
+        }
+        sm.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&sm.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = sm.tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int it = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+                const int mt = t / n_tiles, nt = t % n_tiles;
+                for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(&sm.empty[s], ph ^ 1u, abort, status)) break;
+                    mbar_arrive_tx(&sm.full[s], kA8Bytes + kBBytes);
+                    tma_load_4d(sm.a8[s], &tmA, &sm.full[s], 0, 16 * (ks & 1), ks >> 1, mt * (BM / 4));
+                    tma_load_2d(sm.b[s], &tmB, &sm.full[s], ks * BK, nt * BN);
+                }
+            }
+            // Drain: every issued copy must land before the CTA can exit.
+            for (int k = 0; k < STAGES && it - 1 - k >= 0; ++k) {
+                const int j = it - 1 - k;
+                mbar_wait(&sm.full[j % STAGES], (uint32_t)(j / STAGES) & 1u, abort, status);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int it = 0, lt = 0;
+            for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x, ++lt) {
+                const int acc = lt & 1;
+                const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+                if (!mbar_wait(&sm.tempty[acc], aph ^ 1u, abort, status)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                    if (!mbar_wait(&sm.aready[s], ph, abort, status)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t ad = sdesc_sw128(smem_u32(sm.a[s]));
+                    const uint64_t bd = sdesc_sw128(smem_u32(sm.b[s]));
+#pragma unroll
+                    for (int j = 0; j < BK / 16; ++j)
+                        umma_bf16(d_tmem, ad + (uint64_t)(2 * j), bd + (uint64_t)(2 * j), (ks | j) != 0);
+                    umma_commit(&sm.empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(&sm.tfull[acc]);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------- dequant: int8 -> bf16, swizzled K-major ----------------
+        const int t = threadIdx.x - 128;    // 0..127
+        const int rg = t >> 2, qd = t & 3;  // row group, 16-column quarter
+        int it = 0;
+        for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x) {
+            bool ok = true;
+            for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+                if (!mbar_wait(&sm.full[s], ph, abort, status)) { ok = false; break; }
+                const uint4* src = reinterpret_cast<const uint4*>(sm.a8[s] + rg * 256 + qd * 64);
+                const uint4 c0 = src[0], c1 = src[1], c2 = src[2], c3 = src[3];
+                const uint32_t w[4][4] = {{c0.x, c1.x, c2.x, c3.x},
+                                          {c0.y, c1.y, c2.y, c3.y},
+                                          {c0.z, c1.z, c2.z, c3.z},
+                                          {c0.w, c1.w, c2.w, c3.w}};
+#pragma unroll
+                for (int rr = 0; rr < 4; ++rr) {
+                    const int m = rg * 4 + rr;
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) i8x4_to_bf16(w[rr][i], o[2 * i], o[2 * i + 1]);
+                    uint8_t* rowp = sm.a[s] + (m >> 3) * 1024 + (m & 7) * 128;
+                    const int ch0 = (2 * qd) ^ (m & 7), ch1 = (2 * qd + 1) ^ (m & 7);
+                    *reinterpret_cast<uint4*>(rowp + ch0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                    *reinterpret_cast<uint4*>(rowp + ch1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.aready[s]);
+            }
+            if (!ok) break;
+        }
+    } else if (warp >= 8) {
+        // ---------------- epilogue: TMEM -> x rs -> global ----------------
+        const int e = warp & 3;  // TMEM lanes 32e..32e+31
+        int lt = 0;
+        for (int t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x, ++lt) {
+            const int mt = t / n_tiles, nt = t % n_tiles;
+            const int acc = lt & 1;
+            const uint32_t aph = (uint32_t)(lt >> 1) & 1u;
+            if (!mbar_wait(&sm.tfull[acc], aph, abort, status)) break;
+            tc_fence_after();
+            const int row = mt * BM + e * 32 + lane;
+            const float r = row < rows ? rs[row] : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + ((uint32_t)(e * 32) << 16) + (uint32_t)(acc * BN + c * 32), v);
+                const int n0 = nt * BN + c * 32;
+                if (row < rows) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int b = n0 + i;
+                        if (b < nb) y[(size_t)b * rows + row] = r * __uint_as_float(v[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+__global__ void xs_to_bf16_kernel(const float4* __restrict__ xs, uint2* __restrict__ out, int64_t n4) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = xs[i];
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+        out[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+extern "C" qmv_status qmm_q8row(const qmv_weights* w, const float* xs, int64_t nb, float* y, qmv_stream st) {
+    QMV_REQUIRE(w && xs && y, QMV_ERR_INVALID_ARG, "qmm_q8row: null argument");
+    QMV_REQUIRE(w->format == QMV_FMT_Q8ROW, QMV_ERR_UNSUPPORTED, "qmm_q8row: handle is not q8_row");
+    QMV_REQUIRE(w->experts == 1, QMV_ERR_UNSUPPORTED, "qmm_q8row: handle is an expert stack");
+    QMV_REQUIRE(nb >= 1 && nb <= (1 << 20), QMV_ERR_INVALID_ARG, "qmm_q8row: need 1 <= nb <= 2^20");
+    QMV_REQUIRE(qmv::aligned16(xs) && qmv::aligned16(y), QMV_ERR_INVALID_ARG,
+                "qmm_q8row: xs and y must be 16-byte aligned");
+    QMV_REQUIRE(w->rows_pad < (1ll << 31) && w->rows_pad * nb < (1ll << 40), QMV_ERR_UNSUPPORTED,
+                "qmm_q8row: problem too large");
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    QMV_REQUIRE(enc, QMV_ERR_CUDA, "qmm_q8row: cuTensorMapEncodeTiled is unavailable");
+    int* status = qmv::device_status();
+    QMV_REQUIRE(status, QMV_ERR_CUDA, "qmm_q8row: no CUDA device");
+    cudaStream_t cs = (cudaStream_t)st;
+
+    // A: packed int8 codes seen as [rows_pad/4][cols_pad/128][32 lanes][16 bytes].
+    CUtensorMap tmA, tmB;
+    {
+        cuuint64_t dims[4] = {16, 32, (cuuint64_t)(w->cols_pad / 128), (cuuint64_t)(w->rows_pad / 4)};
+        cuuint64_t strides[3] = {16, 512, (cuuint64_t)(4 * w->cols_pad)};
+        cuuint32_t box[4] = {16, 16, 1, BM / 4};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        CUresult r = enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, w->q, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        QMV_REQUIRE(r == CUDA_SUCCESS, QMV_ERR_CUDA, "qmm_q8row: tensor map for W failed (%d)", (int)r);
+    }
+    void* xb = nullptr;
+    const size_t xb_bytes = (size_t)nb * (size_t)w->cols * 2;
+    cudaError_t e = cudaMallocAsync(&xb, xb_bytes, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return qmv::fail(QMV_ERR_ALLOC, "qmm_q8row: scratch allocation failed: %s", cudaGetErrorString(e));
+    }
+    {
+        cuuint64_t dims[2] = {(cuuint64_t)w->cols, (cuuint64_t)nb};
+        cuuint64_t strides[1] = {(cuuint64_t)w->cols * 2};
+        cuuint32_t box[2] = {BK, BN};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xb, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) {
+            cudaFreeAsync(xb, cs);
+            return qmv::fail(QMV_ERR_CUDA, "qmm_q8row: tensor map for xs failed (%d)", (int)r);
+        }
+    }
+    const int64_t n4 = (int64_t)nb * w->cols / 4;
+    int64_t g = (n4 + 255) / 256;
+    if (g > (int64_t)qmv::sm_count() * 8) g = (int64_t)qmv::sm_count() * 8;
+    xs_to_bf16_kernel<<<(unsigned)g, 256, 0, cs>>>(reinterpret_cast<const float4*>(xs), static_cast<uint2*>(xb),
+                                                   n4);
+
+    static int configured[64] = {0};
+    const int dev = qmv::current_device();
+    const size_t smem = sizeof(Smem) + 1024;
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaFuncSetAttribute(qmm_q8row_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        configured[dev] = 1;
+    }
+    const int m_tiles = (int)(w->rows_pad / BM);
+    const int n_tiles = (int)((nb + BN - 1) / BN);
+    const int ksteps = (int)(w->cols_pad / BK);
+    int grid = qmv::sm_count();
+    if (grid > m_tiles * n_tiles) grid = m_tiles * n_tiles;
+    qmm_q8row_tc_kernel<<<grid, kThreads, smem, cs>>>(tmA, tmB, w->rs, y, (int)w->rows, (int)nb, ksteps, m_tiles,
+                                                      n_tiles, status);
+    qmv_status s = qmv::check_launch("qmm_q8row_tc_kernel");
+    cudaFreeAsync(xb, cs);
+    return s;
+}

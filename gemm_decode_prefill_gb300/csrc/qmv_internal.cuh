@@ -1,0 +1,81 @@
+// Internal definitions shared by the libqmv translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "../../include/qmv.h"
+
+// ---------------------------------------------------------------------------
+// Packed weight handle.
+//
+// q8_row layout ("row-group interleaved"): rows are padded to a multiple of
+// kQ8RowPad and columns to a multiple of 128, both zero-filled.  Four
+// consecutive rows form a row group; each row group is a sequence of
+// 128-column blocks of 512 bytes; inside a block, lane l of a warp owns 16
+// bytes = 4 rows x 4 columns (columns 4l..4l+3 of the block), stored row by
+// row.  A warp therefore reads one block as 32 x 16 B = 512 contiguous
+// bytes, and lane l needs activations [128b + 4l, 128b + 4l + 4): one float4,
+// shared by the four rows it holds.
+//   byte(row, col) = rg*(4*cols_pad) + (col/128)*512 + ((col%128)/4)*16
+//                    + (row%4)*4 + col%4,            rg = row/4
+// Expert e of a stack starts at e*rows_pad*cols_pad.  rs is [experts][rows_pad].
+//
+// Q2 layout (mma.sync fragment order): rows padded to a multiple of 32 and
+// columns to a multiple of 128.  A 16-row x 128-column tile is 512 bytes:
+// lane l owns 4 words; bit 2t+16h of word j is the code of
+//   row = (l/4) + 8*(fr&1),  col = 16*s + 2*(l%4) + 8*(fr>>1) + h,
+//   s = 2j + t/4, fr = t%4,
+// i.e. exactly the bf16 A-fragment elements lane l feeds to the
+// m16n8k16 MMA of k-step s.  Tiles are ordered [row tile][column chunk].
+// Scales: per (tile, chunk) 8 x 2 x gpc f16 values ordered
+// [l/4][row half][group in chunk], gpc = 128/group; padded groups have d = 0.
+// ---------------------------------------------------------------------------
+constexpr int kQ8RowPad = 128;
+constexpr int kQ2RowPad = 32;
+
+struct qmv_weights {
+    int format;          // qmv_format
+    int device;          // device ordinal holding the data
+    int group;           // Q2 group size (0 for q8_row)
+    int64_t experts, rows, cols;
+    int64_t rows_pad, cols_pad;
+    int8_t* q;           // q8_row codes (packed)
+    float* rs;           // q8_row row scales [experts][rows_pad]
+    uint4* codes;        // Q2 codes (packed)
+    __half* d;           // Q2 scales (packed)
+    void* base;          // single device allocation
+    int64_t bytes;
+};
+
+namespace qmv {
+
+// Records a one-line error for qmv_last_error() and returns `st`.
+qmv_status fail(qmv_status st, const char* fmt, ...);
+// Maps a pending launch error to QMV_ERR_CUDA.
+qmv_status check_launch(const char* what);
+// Multiprocessor count of the current device (cached).
+int sm_count();
+// Device pointer of the per-device status word (set up on first use).
+int* device_status();
+// Device of the current context.
+int current_device();
+
+// Status codes kernels write into the device status word.
+enum : int {
+    kDevOk = 0,
+    kDevBadExpert = 1,
+    kDevTimeout = 2,
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace qmv
+
+// Validation helpers for the entry points.
+#define QMV_REQUIRE(cond, st, ...)                 \
+    do {                                           \
+        if (!(cond)) return qmv::fail(st, __VA_ARGS__); \
+    } while (0)

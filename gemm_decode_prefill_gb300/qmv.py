@@ -1,0 +1,245 @@
+"""Thin Python binding of libqmv's C ABI (include/qmv.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libqmv.so.  PyTorch provides device memory and streams.  If the
+library has not been built, importing this module raises: there is no
+fallback path.
+
+Names follow the C entry points: ``qmv_pack_q8row``, ``qmv_pack_q2``,
+``qmv_q8row``, ``qmv_q2g64``, ``qmv_q2g128``, ``qmm_q8row``,
+``moe_select_topk``, ``moe_ffn_q8row``, ``qmv_check``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmv.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libqmv.so is not built ({LIB_PATH}); run gemm_decode_prefill_gb300/build.py "
+                      "or __graft_entry__.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+
+_SIGS = {
+    "qmv_status_string": ([_I], ctypes.c_char_p),
+    "qmv_last_error": ([ctypes.c_char_p, ctypes.c_size_t], _I),
+    "qmv_version": ([], _I),
+    "qmv_pack_q8row": ([_P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(_P)], _I),
+    "qmv_pack_q2": ([_P, _P, _I, _I64, _I64, _P, ctypes.POINTER(_P)], _I),
+    "qmv_weights_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                          ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
+    "qmv_weights_free": ([_P], _I),
+    "qmv_q8row": ([_P, _P, _P, _P], _I),
+    "qmv_q2g64": ([_P, _P, _P, _P], _I),
+    "qmv_q2g128": ([_P, _P, _P, _P], _I),
+    "qmm_q8row": ([_P, _P, _I64, _P, _P], _I),
+    "moe_select_topk": ([_P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P], _I),
+    "moe_ffn_q8row": ([_P, _P, _P, _P, _P, _I, _P, _P, _P], _I),
+    "qmv_check": ([_P, ctypes.POINTER(_I)], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+EXPORTS = tuple(_SIGS)
+
+FMT_Q8ROW, FMT_Q2G64, FMT_Q2G128 = 1, 2, 3
+
+
+class QmvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        buf = ctypes.create_string_buffer(512)
+        _lib.qmv_last_error(buf, 512)
+        self.status = status
+        name = _lib.qmv_status_string(status).decode()
+        super().__init__(f"{where}: {name}: {buf.value.decode(errors='replace')}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise QmvError(status, where)
+
+
+def status_string(status: int) -> str:
+    return _lib.qmv_status_string(status).decode()
+
+
+def version() -> int:
+    return _lib.qmv_version()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Weights:
+    """Library-owned packed weights (a ``qmv_weights*``)."""
+
+    def __init__(self, handle: int, fmt: int, experts: int, rows: int, cols: int, nbytes: int):
+        self._h = ctypes.c_void_p(handle)
+        self.format = fmt
+        self.experts = experts
+        self.rows = rows
+        self.cols = cols
+        self.device_bytes = nbytes
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise ValueError("weights handle already freed")
+        return self._h
+
+    def free(self):
+        if self._h:
+            h, self._h = self._h, ctypes.c_void_p(0)
+            _check(_lib.qmv_weights_free(h), "qmv_weights_free")
+
+    def __del__(self):
+        try:
+            if self._h:
+                _lib.qmv_weights_free(self._h)
+                self._h = ctypes.c_void_p(0)
+        except Exception:
+            pass
+
+
+def _wrap(h: ctypes.c_void_p) -> Weights:
+    fmt = _I(); e = _I64(); r = _I64(); c = _I64(); b = _I64()
+    _check(_lib.qmv_weights_info(h, ctypes.byref(fmt), ctypes.byref(e), ctypes.byref(r),
+                                 ctypes.byref(c), ctypes.byref(b)), "qmv_weights_info")
+    return Weights(h.value, fmt.value, e.value, r.value, c.value, b.value)
+
+
+def qmv_pack_q8row(q: torch.Tensor, rs: torch.Tensor, stream=None) -> Weights:
+    """q: int8 [rows][cols] or [experts][rows][cols]; rs: f32 [rows] / [experts][rows]."""
+    if q.dim() == 2:
+        experts, (rows, cols) = 1, q.shape
+    elif q.dim() == 3:
+        experts, rows, cols = q.shape
+    else:
+        raise ValueError("q must be 2-D or 3-D")
+    qp = _dev(q, torch.int8, "q")
+    rp = _dev(rs, torch.float32, "rs", (rows,) if q.dim() == 2 else (experts, rows))
+    h = ctypes.c_void_p()
+    _check(_lib.qmv_pack_q8row(qp, rp, experts, rows, cols, _stream(stream), ctypes.byref(h)),
+           "qmv_pack_q8row")
+    return _wrap(h)
+
+
+def qmv_pack_q2(codes: torch.Tensor, d_bits: torch.Tensor, group: int, stream=None) -> Weights:
+    """codes: uint8 [rows][cols/4]; d_bits: f16 bit patterns as int16/uint16 or float16 [rows][cols/group]."""
+    rows, cb = codes.shape
+    cols = cb * 4
+    cp = _dev(codes, torch.uint8, "codes")
+    if d_bits.dtype in (torch.int16, torch.float16) or str(d_bits.dtype) == "torch.uint16":
+        if not d_bits.is_cuda or not d_bits.is_contiguous():
+            raise ValueError("d must be a contiguous CUDA tensor")
+        if group > 0 and tuple(d_bits.shape) != (rows, cols // group):
+            raise ValueError(f"d must have shape {(rows, cols // group)}")
+        dp = ctypes.c_void_p(d_bits.data_ptr())
+    else:
+        raise TypeError("d must hold f16 bit patterns (int16, uint16 or float16)")
+    h = ctypes.c_void_p()
+    _check(_lib.qmv_pack_q2(cp, dp, int(group), rows, cols, _stream(stream), ctypes.byref(h)),
+           "qmv_pack_q2")
+    return _wrap(h)
+
+
+def qmv_q8row(w: Weights, xs: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if y is None:
+        y = torch.empty(w.rows, dtype=torch.float32, device=xs.device)
+    _check(_lib.qmv_q8row(w.handle, _dev(xs, torch.float32, "xs", (w.cols,)),
+                          _dev(y, torch.float32, "y", (w.rows,)), _stream(stream)), "qmv_q8row")
+    return y
+
+
+def _q2(fn, name, w, x, y, stream):
+    if y is None:
+        y = torch.empty(w.rows, dtype=torch.float32, device=x.device)
+    _check(fn(w.handle, _dev(x, torch.float32, "x", (w.cols,)),
+              _dev(y, torch.float32, "y", (w.rows,)), _stream(stream)), name)
+    return y
+
+
+def qmv_q2g64(w: Weights, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _q2(_lib.qmv_q2g64, "qmv_q2g64", w, x, y, stream)
+
+
+def qmv_q2g128(w: Weights, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    return _q2(_lib.qmv_q2g128, "qmv_q2g128", w, x, y, stream)
+
+
+def qmm_q8row(w: Weights, xs: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    nb = xs.shape[0]
+    if y is None:
+        y = torch.empty(nb, w.rows, dtype=torch.float32, device=xs.device)
+    _check(_lib.qmm_q8row(w.handle, _dev(xs, torch.float32, "xs", (nb, w.cols)), nb,
+                          _dev(y, torch.float32, "y", (nb, w.rows)), _stream(stream)), "qmm_q8row")
+    return y
+
+
+def moe_select_topk(logits: torch.Tensor, top_k: int, renorm: bool, sg_w: torch.Tensor | None = None,
+                    x: torch.Tensor | None = None, sg_logit: torch.Tensor | None = None,
+                    sel: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None):
+    n = logits.shape[0]
+    slots = top_k + (1 if (sg_w is not None or sg_logit is not None) else 0)
+    dev = logits.device
+    if sel is None:
+        sel = torch.empty(slots, dtype=torch.int32, device=dev)
+    if w is None:
+        w = torch.empty(slots, dtype=torch.float32, device=dev)
+    hidden = 0
+    sgp = xp = slp = None
+    if sg_w is not None:
+        hidden = sg_w.shape[0]
+        sgp = _dev(sg_w, torch.float32, "sg_w")
+        xp = _dev(x, torch.float32, "x", (hidden,))
+    elif sg_logit is not None:
+        slp = _dev(sg_logit, torch.float32, "sg_logit", (1,))
+    _check(_lib.moe_select_topk(_dev(logits, torch.float32, "logits", (n,)), n, int(top_k), int(bool(renorm)),
+                                sgp, xp, hidden, slp, _dev(sel, torch.int32, "sel", (slots,)),
+                                _dev(w, torch.float32, "w", (slots,)), _stream(stream)), "moe_select_topk")
+    return sel, w
+
+
+def moe_ffn_q8row(gate: Weights, up: Weights, down: Weights, sel: torch.Tensor, w: torch.Tensor,
+                  x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    slots = sel.shape[0]
+    if out is None:
+        out = torch.empty(gate.cols, dtype=torch.float32, device=x.device)
+    _check(_lib.moe_ffn_q8row(gate.handle, up.handle, down.handle, _dev(sel, torch.int32, "sel", (slots,)),
+                              _dev(w, torch.float32, "w", (slots,)), slots,
+                              _dev(x, torch.float32, "x", (gate.cols,)),
+                              _dev(out, torch.float32, "out", (gate.cols,)), _stream(stream)), "moe_ffn_q8row")
+    return out
+
+
+def qmv_check(stream=None) -> int:
+    """Reads and clears the device status word; raises QmvError if it was set."""
+    code = _I(0)
+    _check(_lib.qmv_check(_stream(stream), ctypes.byref(code)), "qmv_check")
+    return code.value

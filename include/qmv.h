@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -63,14 +69,14 @@ typedef enum {
 typedef struct qmv_weights qmv_weights; /* opaque, library-owned */
 
 /* Static, never-NULL name of a status code. */
-const char *qmv_status_string(int status);
+QMV_API const char *qmv_status_string(int status);
 
 /* Copies the calling thread's last error message (host buffer `buf` of `n`
  * bytes, always NUL-terminated when n > 0).  Returns the status it belongs to. */
-int qmv_last_error(char *buf, size_t n);
+QMV_API int qmv_last_error(char *buf, size_t n);
 
 /* ABI version (major * 100 + minor). */
-int qmv_version(void);
+QMV_API int qmv_version(void);
 
 /* ---------------------------------------------------------------------- */
 /* Load-time repack (done once per weight tensor; not on the per-token path) */
@@ -85,7 +91,7 @@ int qmv_version(void);
  * Writes a new handle to *out (host pointer).
  * (Repack at load time: qxmx_gpu.cpp, `upload_q2`, which reorders the
  * weights once at upload so that the hot loop reads them in order.) */
-qmv_status qmv_pack_q8row(const int8_t *q, const float *rs, int64_t experts,
+QMV_API qmv_status qmv_pack_q8row(const int8_t *q, const float *rs, int64_t experts,
                           int64_t rows, int64_t cols, qmv_stream st,
                           qmv_weights **out);
 
@@ -96,17 +102,17 @@ qmv_status qmv_pack_q8row(const int8_t *q, const float *rs, int64_t experts,
  * Same ownership rules as qmv_pack_q8row.
  * (qxmx_gpu.cpp, `dequant_embd` for the bit order, `repack_q2_g64`,
  * `repack_q2_g128` and `upload_q2` for the load-time repack.) */
-qmv_status qmv_pack_q2(const uint8_t *codes, const uint16_t *d, int group,
+QMV_API qmv_status qmv_pack_q2(const uint8_t *codes, const uint16_t *d, int group,
                        int64_t rows, int64_t cols, qmv_stream st,
                        qmv_weights **out);
 
 /* Describes a handle (host out-pointers, each may be NULL). */
-qmv_status qmv_weights_info(const qmv_weights *w, int *format, int64_t *experts,
+QMV_API qmv_status qmv_weights_info(const qmv_weights *w, int *format, int64_t *experts,
                             int64_t *rows, int64_t *cols, int64_t *device_bytes);
 
 /* Frees a handle (NULL is a no-op).  Synchronizes the device first, so
  * work already enqueued that reads the handle completes. */
-qmv_status qmv_weights_free(qmv_weights *w);
+QMV_API qmv_status qmv_weights_free(qmv_weights *w);
 
 /* ---------------------------------------------------------------------- */
 /* Decode GEMVs                                                           */
@@ -117,7 +123,7 @@ qmv_status qmv_weights_free(qmv_weights *w);
  * fp32 arithmetic on exactly converted int8 codes; deterministic.
  * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `q8_matvec`; cortiq-engine
  * 0.3.7 src/gpu_metal.rs, MSL `q8_matvec`.) */
-qmv_status qmv_q8row(const qmv_weights *w, const float *xs, float *y,
+QMV_API qmv_status qmv_q8row(const qmv_weights *w, const float *xs, float *y,
                      qmv_stream st);
 
 /* y[m] = sum_g d[m,g] * sum_{k in g} (q[m,k] - 1) * x[k] for a Q2 g64
@@ -127,9 +133,9 @@ qmv_status qmv_q8row(const qmv_weights *w, const float *xs, float *y,
  * The K dimension is split across warps and the partial sums are reduced
  * in a fixed order (deterministic).
  * (qxmx_gpu.cpp, `gemv_dpas8` and its split-K reduce `gemv_reduce`.) */
-qmv_status qmv_q2g64(const qmv_weights *w, const float *x, float *y,
+QMV_API qmv_status qmv_q2g64(const qmv_weights *w, const float *x, float *y,
                      qmv_stream st);
-qmv_status qmv_q2g128(const qmv_weights *w, const float *x, float *y,
+QMV_API qmv_status qmv_q2g128(const qmv_weights *w, const float *x, float *y,
                       qmv_stream st);
 
 /* ---------------------------------------------------------------------- */
@@ -144,7 +150,7 @@ qmv_status qmv_q2g128(const qmv_weights *w, const float *x, float *y,
  * result.  Uses a stream-ordered scratch allocation of nb*cols*2 bytes.
  * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `q8_matmat` and `q8_mul_mm`;
  * cortiq-engine 0.3.7 src/gpu_metal.rs, MSL `q8_mul_mm`.) */
-qmv_status qmm_q8row(const qmv_weights *w, const float *xs, int64_t nb,
+QMV_API qmv_status qmm_q8row(const qmv_weights *w, const float *xs, int64_t nb,
                      float *y, qmv_stream st);
 
 /* ---------------------------------------------------------------------- */
@@ -163,7 +169,7 @@ qmv_status qmm_q8row(const qmv_weights *w, const float *xs, int64_t nb,
  *   Outputs: sel [top_k(+1)] int32, w [top_k(+1)] f32.
  * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_select_sg` and
  * `moe_select`.) */
-qmv_status moe_select_topk(const float *logits, int n_exp, int top_k,
+QMV_API qmv_status moe_select_topk(const float *logits, int n_exp, int top_k,
                            int renorm, const float *sg_w, const float *x,
                            int hidden, const float *sg_logit, int32_t *sel,
                            float *w, qmv_stream st);
@@ -179,7 +185,7 @@ qmv_status moe_select_topk(const float *logits, int n_exp, int top_k,
  * Uses a stream-ordered scratch allocation of slots*inter*4 bytes.
  * (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_gate_up` and `moe_down`;
  * cortiq-engine 0.3.7 src/gpu_metal.rs, host `moe_block`.) */
-qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
+QMV_API qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
                          const qmv_weights *down, const int32_t *sel,
                          const float *w, int slots, const float *x,
                          float *out, qmv_stream st);
@@ -188,7 +194,7 @@ qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
  * a violated invariant (e.g. an expert id out of range).  Synchronizes `st`.
  * Returns QMV_OK or QMV_ERR_DEVICE_STATUS (*code gets the first reason,
  * host pointer, may be NULL). */
-qmv_status qmv_check(qmv_stream st, int *code);
+QMV_API qmv_status qmv_check(qmv_stream st, int *code);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,139 @@
+"""Decode GEMVs (q8_row and Q2 g64/g128) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_decode_prefill_gb300 import synth
+from gpu_helpers import TOL_GEMV, assert_within, d16, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qmv():
+    from gemm_decode_prefill_gb300 import qmv as m
+    return m
+
+
+# ------------------------------------------------------------------ q8_row
+
+Q8_SHAPES = [(1, 16), (5, 48), (37, 128), (64, 144), (300, 640), (129, 1040), (1000, 4096), (4096, 4096)]
+
+
+@pytest.mark.parametrize("rows,cols", Q8_SHAPES)
+def test_q8row_matches_oracle(qmv, rows, cols):
+    q, rs, xs = synth.q8_inputs(rows, cols, seed=rows * 7 + cols)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmv_q8row(w, dev(xs)))
+    y_ref, mag = oracle.q8row(q, rs, xs, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMV, f"q8row {rows}x{cols}")
+
+
+def test_q8row_exact_integer_case_is_bit_exact(qmv):
+    g = synth.rng(31)
+    rows, cols = 4096, 4096
+    q = g.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+    xs = g.integers(-2, 3, size=cols).astype(np.float32)
+    rs = (2.0 ** g.integers(-6, 2, size=rows)).astype(np.float32)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmv_q8row(w, dev(xs)))
+    assert np.array_equal(y.astype(np.float64), oracle.q8row(q, rs, xs))
+
+
+def test_q8row_full_lm_head(qmv):
+    cfg = synth.WORKLOADS["q8_lm_head_151936x4096"]
+    q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmv_q8row(w, dev(xs)))
+    y_ref, mag = oracle.q8row(q, rs, xs, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMV, "q8row lm_head 151936x4096")
+
+
+def test_q8row_is_deterministic_and_does_not_write_outside(qmv):
+    q, rs, xs = synth.q8_inputs(333, 512, seed=3)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    buf = torch.full((333 + 64,), float("nan"), device="cuda")
+    y1 = qmv.qmv_q8row(w, dev(xs), buf[:333])
+    a = host(y1).copy()
+    qmv.qmv_q8row(w, dev(xs), buf[:333])
+    b = host(buf)
+    assert np.array_equal(a, b[:333])
+    assert np.isnan(b[333:]).all()  # guard band untouched
+
+
+# --------------------------------------------------------------------- Q2
+
+Q2_SHAPES = [(1, 128), (17, 128), (33, 192), (100, 640), (257, 1024), (1000, 5120)]
+
+
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("rows,cols", Q2_SHAPES)
+def test_q2_matches_oracle(qmv, group, rows, cols):
+    if cols % group:
+        pytest.skip("cols not a multiple of the group")
+    codes, d, x = synth.q2_inputs(rows, cols, group, seed=rows + cols + group)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+    fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+    y = host(fn(w, dev(x)))
+    y_ref, mag = oracle.q2(codes, d, group, x, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMV, f"q2 g{group} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_full_config(qmv, group):
+    cfg = synth.WORKLOADS["q2_gemv_17408x5120"]
+    codes, d, x = synth.q2_inputs(cfg["rows"], cfg["cols"], group, cfg["seed"])
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+    fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+    y = host(fn(w, dev(x)))
+    y_ref, mag = oracle.q2(codes, d, group, x, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMV, f"q2 g{group} 17408x5120")
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_exact_integer_case_is_bit_exact(qmv, group):
+    g = synth.rng(41 + group)
+    rows, cols = 1088, 5120
+    codes = g.integers(0, 256, size=(rows, cols // 4), dtype=np.uint8)
+    d = (2.0 ** g.integers(-4, 2, size=(rows, cols // group))).astype(np.float16).view(np.uint16)
+    x = g.integers(-3, 4, size=cols).astype(np.float32)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+    fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+    y = host(fn(w, dev(x)))
+    assert np.array_equal(y.astype(np.float64), oracle.q2(codes, d, group, x))
+
+
+def test_q2_unit_vector_probe(qmv):
+    """x = e_j returns the single dequantised weight column: pins the packed
+    bit order and fragment mapping for every column of two chunks."""
+    codes, d, _ = synth.q2_inputs(48, 256, 64, seed=51)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), 64)
+    dd = d.view(np.float16).astype(np.float64)
+    for j in range(256):
+        x = np.zeros(256, np.float32); x[j] = 1.0
+        y = host(qmv.qmv_q2g64(w, dev(x)))
+        q = (codes[:, j // 4] >> (2 * (j % 4))) & 3
+        assert np.array_equal(y.astype(np.float64), dd[:, j // 64] * (q.astype(np.float64) - 1.0)), j
+
+
+def test_q2_g128_equals_two_g64_on_gpu(qmv):
+    codes, d128, x = synth.q2_inputs(777, 2048, 128, seed=52)
+    d64 = np.repeat(d128, 2, axis=1)
+    w128 = qmv.qmv_pack_q2(dev(codes), d16(d128), 128)
+    w64 = qmv.qmv_pack_q2(dev(codes), d16(d64), 64)
+    y128 = host(qmv.qmv_q2g128(w128, dev(x)))
+    y64 = host(qmv.qmv_q2g64(w64, dev(x)))
+    _, mag = oracle.q2(codes, d128, 128, x, with_mag=True)
+    assert_within(y128, y64.astype(np.float64), mag, 2 * TOL_GEMV, "g128 vs 2xg64")
+
+
+def test_q2_wrong_group_entry_point_is_rejected(qmv):
+    codes, d, x = synth.q2_inputs(32, 128, 64, seed=53)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), 64)
+    with pytest.raises(qmv.QmvError, match="UNSUPPORTED"):
+        qmv.qmv_q2g128(w, dev(x))
+    q8, rs, xs = synth.q8_inputs(32, 128, seed=54)
+    w8 = qmv.qmv_pack_q8row(dev(q8), dev(rs))
+    with pytest.raises(qmv.QmvError, match="UNSUPPORTED"):
+        qmv.qmv_q2g64(w8, dev(x))

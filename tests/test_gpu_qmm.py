@@ -1,0 +1,83 @@
+"""Prefill GEMM (tcgen05) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_decode_prefill_gb300 import synth
+from gpu_helpers import TOL_GEMM, assert_within, dev, host
+
+pytestmark = pytest.mark.gpu
+
+# Diagnostic bound against the bf16-rounded-xs twin: only fp32 accumulation
+# differs, so indexing errors cannot hide inside the bf16 tolerance.
+TOL_TWIN = 1e-5
+
+
+@pytest.fixture(scope="module")
+def qmv():
+    from gemm_decode_prefill_gb300 import qmv as m
+    return m
+
+
+QMM_SHAPES = [(1, 128, 1), (128, 128, 7), (300, 640, 33), (256, 1040, 256), (384, 256, 300), (129, 2048, 513)]
+
+
+@pytest.mark.parametrize("rows,cols,nb", QMM_SHAPES)
+def test_qmm_matches_oracle_and_bf16_twin(qmv, rows, cols, nb):
+    q, rs, xs = synth.qmm_inputs(rows, cols, nb, seed=rows + cols + nb)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmm_q8row(w, dev(xs)))
+    y_ref, mag = oracle.qmm(q, rs, xs, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMM, f"qmm {rows}x{cols} nb={nb}")
+    y_twin, mag_twin = oracle.qmm(q, rs, xs, with_mag=True, bf16_xs=True)
+    assert_within(y, y_twin, mag_twin, TOL_TWIN, f"qmm twin {rows}x{cols} nb={nb}")
+
+
+def test_qmm_exact_integer_case_is_bit_exact(qmv):
+    g = synth.rng(61)
+    rows, cols, nb = 512, 2048, 300
+    q = g.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+    xs = g.integers(-2, 3, size=(nb, cols)).astype(np.float32)
+    rs = (2.0 ** g.integers(-6, 2, size=rows)).astype(np.float32)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmm_q8row(w, dev(xs)))
+    assert np.array_equal(y.astype(np.float64), oracle.qmm(q, rs, xs))
+
+
+def test_qmm_nb1_matches_q8row_bound(qmv):
+    q, rs, xs = synth.qmm_inputs(256, 512, 1, seed=62)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmm_q8row(w, dev(xs)))[0]
+    y_ref, mag = oracle.q8row(q, rs, xs[0], with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMM, "qmm nb=1")
+
+
+def test_qmm_full_config_sampled_rows(qmv):
+    cfg = synth.WORKLOADS["q8_prefill_gemm_17408x5120_nb512"]
+    q, rs, xs = synth.qmm_inputs(cfg["rows"], cfg["cols"], cfg["nb"], cfg["seed"])
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    y = host(qmv.qmm_q8row(w, dev(xs)))
+    assert y.shape == (512, 17408) and np.isfinite(y).all()
+    g = synth.rng(63)
+    # every M tile's first and last row, plus random rows: all 512 tokens each
+    rows = np.unique(np.concatenate([np.arange(0, 17408, 128), np.arange(127, 17408, 128),
+                                     g.integers(0, 17408, size=64)]))
+    y_ref, mag = oracle.qmm(q[rows], rs[rows], xs, with_mag=True)
+    assert_within(y[:, rows], y_ref, mag, TOL_GEMM, "qmm 17408x5120 nb=512 (sampled rows)")
+    y_twin, mag_twin = oracle.qmm(q[rows], rs[rows], xs, with_mag=True, bf16_xs=True)
+    assert_within(y[:, rows], y_twin, mag_twin, TOL_TWIN, "qmm twin (sampled rows)")
+
+
+def test_qmm_guard_band_and_repeatability(qmv):
+    q, rs, xs = synth.qmm_inputs(200, 384, 40, seed=64)
+    w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    buf = torch.full((40 * 200 + 1024,), float("nan"), device="cuda")
+    out = buf[:40 * 200].view(40, 200)
+    qmv.qmm_q8row(w, dev(xs), out)
+    a = host(out).copy()
+    qmv.qmm_q8row(w, dev(xs), out)
+    b = host(buf)
+    assert np.array_equal(a.reshape(-1), b[:40 * 200])
+    assert np.isnan(b[40 * 200:]).all()
+    assert qmv.qmv_check() == 0
