@@ -1,0 +1,608 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized decode/prefill hot path on GB300.
+
+Headline workload: the Q2 (2-bit group) decode GEMV, M=17408, K=5120, in
+both the g64 and the g128 layout.  One step = one g64 GEMV + one g128 GEMV
+(split-K reduction included) over the same activation vector.  The metric is
+weight GB/s: algorithmic bytes (codes + scales + x + y) per step / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rules followed: W untimed warm-up steps; exactly K timed steps bracketed by
+a barrier and torch.cuda.synchronize(); CUDA events on the launching
+stream; the max over ranks; inputs larger than L2 (8 rotated copies of the
+packed weights of each layout); nvidia-smi clocks sampled during the timed
+region.  Multi-GPU: replicas only (one independent workload per rank, no
+collective on the data path), weak scaling.
+
+Extra measurements (``rows``): the other workloads of the hot path, each
+timed the same way: q8_row GEMV 4096x4096, lm_head 151936x4096, the tcgen05
+prefill GEMM 17408x5120 nb=512, and the MoE decode step.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload per step (rank 0 only under torchrun).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode GEMV weight GB/s (% of HBM peak); prefill GEMM TFLOP/s (% tensor peak)"
+Q2_ROWS, Q2_COLS = 17408, 5120
+L2_BYTES = 129 * 1024 * 1024
+Q2_COPIES = 8
+GRAPH_STEPS = 96          # steps per captured graph (a multiple of Q2_COPIES)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def q2_bytes(rows: int, cols: int, group: int) -> int:
+    """Codes + f16 scales + x (f32) + y (f32)."""
+    return rows * cols // 4 + rows * (cols // group) * 2 + cols * 4 + rows * 4
+
+
+def q8_bytes(rows: int, cols: int) -> int:
+    """Codes + rs + xs + y."""
+    return rows * cols + rows * 4 + cols * 4 + rows * 4
+
+
+def qmm_flops(rows: int, cols: int, nb: int) -> int:
+    return 2 * rows * cols * nb
+
+
+def moe_bytes(slots: int, hidden: int, inter: int) -> int:
+    """Selected experts' gate+up+down codes and scales, plus x, logits-sized vectors and out."""
+    per = 2 * inter * hidden + hidden * inter + 2 * inter * 4 + hidden * 4
+    return slots * per + hidden * 4 * 2
+
+
+STEP_BYTES = q2_bytes(Q2_ROWS, Q2_COLS, 64) + q2_bytes(Q2_ROWS, Q2_COLS, 128)
+
+
+# ------------------------------------------------------------------ peaks, clocks, traffic
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def mark(self, begin: bool):
+        self.windows.append((time.time(), begin))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm = float(parts[1].split()[0])
+                    mx = float(parts[2].split()[0])
+                except ValueError:
+                    continue
+                rows.append((sm, mx, parts[5:9]))
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        loaded = [sm for sm, _, _ in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx for _, mx, _ in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_digest(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+Q2_SOURCES = ["gemm_decode_prefill_gb300/csrc/gemv_q2.cu", "gemm_decode_prefill_gb300/csrc/qmv_internal.cuh"]
+
+
+def recorded_traffic(kernel_tag: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    this exact kernel source (profiles/*.md lines `traffic: <tag> <bytes> <digest>`)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, fn)) as f:
+            for line in f:
+                m = re.match(r"\s*traffic:\s+(\S+)\s+(\d+)\s+(\w+)", line)
+                if m and m.group(1) == kernel_tag and m.group(3) == digest:
+                    return int(m.group(2))
+    return None
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, ws, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(v: float) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return v
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(elapsed_s: float, units_per_rank: float, world: int):
+    """Whole-job throughput: all ranks' units / the slowest rank's time."""
+    t = reduce_max(elapsed_s)
+    return units_per_rank * world / t, t
+
+
+# ------------------------------------------------------------------ GPU timing helpers
+
+def graph_of(fn, n: int, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(0)   # one eager call before capture (first-use set-up happens here)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                fn(i)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, replays: int, stream) -> float:
+    """Seconds for `replays` replays of graph g, CUDA events on `stream`."""
+    import torch
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / 1e3
+
+
+def kernel_time(fn, launches_per_graph: int, stream, min_seconds: float = 0.3):
+    """Average seconds per launch of fn over graphs of `launches_per_graph` launches."""
+    g = graph_of(fn, launches_per_graph, stream)
+    t = time_graph(g, 2, stream)  # warm
+    reps = max(3, int(min_seconds / max(t / 2, 1e-6)))
+    t = time_graph(g, reps, stream)
+    return t / (reps * launches_per_graph)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    import torch
+    import oracle  # CPU-baseline leg and the parity spot check only
+    from gemm_decode_prefill_gb300 import qmv, synth
+
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    dev = torch.device("cuda", local)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # --- the Q2 workload: both layouts, rotated copies (> L2) ---
+    seed = synth.WORKLOADS["q2_gemv_17408x5120"]["seed"]
+    host = {}
+    W = {64: [], 128: []}
+    for group in (64, 128):
+        codes, d, x = synth.q2_inputs(Q2_ROWS, Q2_COLS, group, seed)
+        host[group] = (codes, d, x)
+        c_dev, d_dev = up(codes), up(d.view(np.int16))
+        for _ in range(Q2_COPIES):
+            W[group].append(qmv.qmv_pack_q2(c_dev, d_dev, group, stream=stream))
+        del c_dev, d_dev
+    x_dev = up(host[64][2])
+    y64 = torch.empty(Q2_ROWS, device=dev)
+    y128 = torch.empty(Q2_ROWS, device=dev)
+    torch.cuda.synchronize()
+
+    def step(i):
+        c = i % Q2_COPIES
+        qmv.qmv_q2g64(W[64][c], x_dev, y64, stream=stream)
+        qmv.qmv_q2g128(W[128][c], x_dev, y128, stream=stream)
+
+    # parity spot check of the benchmarked configuration (full outputs)
+    with torch.cuda.stream(stream):
+        step(0)
+    torch.cuda.synchronize()
+    parity = {}
+    for group, y in ((64, y64), (128, y128)):
+        codes, d, x = host[group]
+        ref, mag = oracle.q2(codes, d, group, x, with_mag=True)
+        err = np.abs(y.cpu().numpy().astype(np.float64) - ref)
+        parity[f"q2g{group}_max_err_over_bound"] = float(np.max(err / (1e-5 * mag)))
+
+    # --- warm-up, then exactly K timed steps ---
+    for i in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step(i)
+    torch.cuda.synchronize()
+    gsteps = GRAPH_STEPS
+    g = graph_of(step, gsteps, stream)
+    replays, rem = divmod(args.steps, gsteps)
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(replays):
+        g.replay()
+    with torch.cuda.stream(stream):
+        for i in range(rem):
+            step(i)
+    e.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    elapsed = s.elapsed_time(e) / 1e3
+
+    # --- per-kernel roofline (each Q2 kernel alone, same rotation) ---
+    def only64(i):
+        qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y64, stream=stream)
+
+    def only128(i):
+        qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y128, stream=stream)
+
+    t64 = kernel_time(only64, gsteps, stream, min_seconds=1.0)
+    t128 = kernel_time(only128, gsteps, stream, min_seconds=1.0)
+    clk = clocks.stop()
+
+    value, tmax = aggregate(elapsed, STEP_BYTES * args.steps / 1e9, world)
+    dom = 64 if t64 >= t128 else 128
+    tdom = t64 if dom == 64 else t128
+    ach = q2_bytes(Q2_ROWS, Q2_COLS, dom) / tdom / 1e9
+    digest = source_digest(Q2_SOURCES)
+    roofline = {"bound": "hbm", "kernel": f"q2_gemv_kernel<{dom}>", "achieved": round(ach, 1),
+                "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic(f"q2_gemv_kernel<{dom}>", digest),
+                "other": {"kernel": f"q2_gemv_kernel<{192 - dom}>",
+                          "achieved": round(q2_bytes(Q2_ROWS, Q2_COLS, 192 - dom) / (t128 if dom == 64 else t64) / 1e9, 1)},
+                "source_digest": digest}
+
+    # --- end to end through the public API with host buffers ---
+    e2e = run_e2e(args, qmv, W, host, dev, stream)
+
+    # --- the other rows of the hot path ---
+    rows = {}
+    if not args.no_rows:
+        rows = measure_rows(qmv, synth, up, dev, stream, peaks)
+
+    # --- oracle on the host cores (rank 0, N = 1 only) ---
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(oracle, host, min_seconds=args.cpu_seconds)
+
+    del g
+    for group in (64, 128):
+        for w in W[group]:
+            w.free()
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tmax / args.steps * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "q2_gemv_17408x5120_g64+g128", "rows": Q2_ROWS, "cols": Q2_COLS,
+                   "groups": [64, 128], "step": "one g64 GEMV + one g128 GEMV (split-K reduce included)",
+                   "bytes_per_step": STEP_BYTES,
+                   "l2": f"inputs larger than L2: {Q2_COPIES} rotated packed copies per layout "
+                         f"({Q2_COPIES * STEP_BYTES / 1e6:.0f} MB > 129 MB)",
+                   "parallelism": f"replicas x{world}", "launch": f"CUDA graph of {GRAPH_STEPS} steps"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "parity": parity,
+        "rows": rows,
+        "impl": "ours",
+    }
+    return line
+
+
+def run_e2e(args, qmv, W, host, dev, stream):
+    """The same metric through the public API, host buffers in and out: per
+    step the pinned host x goes to the device, both GEMVs run, both y come back."""
+    import torch
+    x_host = torch.from_numpy(host[64][2].copy()).pin_memory()
+    y_host = torch.empty(2, Q2_ROWS, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty(Q2_COLS, device=dev)
+    y_dev = torch.empty(2, Q2_ROWS, device=dev)
+    n = max(50, min(args.steps, 2000))
+    for i in range(5):
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y_dev[0], stream=stream)
+            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y_dev[1], stream=stream)
+            y_host.copy_(y_dev, non_blocking=True)
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    s.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            x_dev.copy_(x_host, non_blocking=True)
+            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y_dev[0], stream=stream)
+            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y_dev[1], stream=stream)
+            y_host.copy_(y_dev, non_blocking=True)
+    e.record(stream)
+    torch.cuda.synchronize()
+    t = s.elapsed_time(e) / 1e3
+    v, _ = aggregate(t, STEP_BYTES * n / 1e9, int(os.environ.get("WORLD_SIZE", "1")))
+    return {"value": round(v, 1), "unit": "GB/s", "steps": n, "h2d_bytes_per_step": Q2_COLS * 4,
+            "d2h_bytes_per_step": 2 * Q2_ROWS * 4, "path": "qmv.qmv_q2g64 + qmv.qmv_q2g128 (C ABI), eager"}
+
+
+def measure_rows(qmv, synth, up, dev, stream, peaks):
+    import torch
+    out = {}
+    hbm = peaks["hbm_gbs"]
+
+    # q8_row GEMV 4096 x 4096: 16 rotated copies (> 2x L2)
+    cfg = synth.WORKLOADS["q8_gemv_4096x4096"]
+    q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
+    qd, rd = up(q), up(rs)
+    ws = [qmv.qmv_pack_q8row(qd, rd, stream=stream) for _ in range(16)]
+    xd = up(xs)
+    y = torch.empty(cfg["rows"], device=dev)
+    t = kernel_time(lambda i: qmv.qmv_q8row(ws[i % 16], xd, y, stream=stream), 160, stream)
+    b = q8_bytes(cfg["rows"], cfg["cols"])
+    out["q8_gemv_4096x4096"] = {"kernel": "q8row_gemv_kernel", "us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                                "frac_hbm": round(b / t / 1e9 / hbm, 4), "bytes": b, "l2": "16 rotated copies"}
+    for w_ in ws:
+        w_.free()
+    del qd, rd
+
+    # lm_head 151936 x 4096 (622 MB > L2)
+    cfg = synth.WORKLOADS["q8_lm_head_151936x4096"]
+    q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
+    w = qmv.qmv_pack_q8row(up(q), up(rs), stream=stream)
+    del q
+    xd = up(xs)
+    y = torch.empty(cfg["rows"], device=dev)
+    t = kernel_time(lambda i: qmv.qmv_q8row(w, xd, y, stream=stream), 20, stream)
+    b = q8_bytes(cfg["rows"], cfg["cols"])
+    out["q8_lm_head_151936x4096"] = {"kernel": "q8row_gemv_kernel", "us": round(t * 1e6, 3),
+                                     "GB/s": round(b / t / 1e9, 1), "frac_hbm": round(b / t / 1e9 / hbm, 4),
+                                     "bytes": b, "l2": "622 MB weights > L2"}
+    w.free()
+
+    # prefill GEMM 17408 x 5120, nb = 512: 4 rotated weight copies
+    cfg = synth.WORKLOADS["q8_prefill_gemm_17408x5120_nb512"]
+    q, rs, xs = synth.qmm_inputs(cfg["rows"], cfg["cols"], cfg["nb"], cfg["seed"])
+    qd, rd = up(q), up(rs)
+    ws = [qmv.qmv_pack_q8row(qd, rd, stream=stream) for _ in range(4)]
+    del qd, rd
+    xd = up(xs)
+    y = torch.empty(cfg["nb"], cfg["rows"], device=dev)
+    t = kernel_time(lambda i: qmv.qmm_q8row(ws[i % 4], xd, y, stream=stream), 8, stream, min_seconds=1.0)
+    fl = qmm_flops(cfg["rows"], cfg["cols"], cfg["nb"])
+    tf = fl / t / 1e12
+    out["q8_prefill_gemm_17408x5120_nb512"] = {
+        "kernel": "qmm_q8row_tc_kernel (+ xs_to_bf16_kernel)", "us": round(t * 1e6, 2), "TFLOP/s": round(tf, 1),
+        "frac_bf16_burst": round(tf / peaks["bf16_tflops"], 4),
+        "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4), "flops": fl,
+        "l2": "4 rotated weight copies (356 MB)"}
+    for w_ in ws:
+        w_.free()
+
+    # MoE decode step: select + gate/up + down, 64 rotated logit vectors
+    cfg = synth.WORKLOADS["moe_decode_h2048_e128_k8"]
+    m = synth.moe_inputs(cfg["n_exp"], cfg["hidden"], cfg["inter"], cfg["seed"])
+    gate = qmv.qmv_pack_q8row(up(m.gq), up(m.grs), stream=stream)
+    upw = qmv.qmv_pack_q8row(up(m.uq), up(m.urs), stream=stream)
+    down = qmv.qmv_pack_q8row(up(m.dq), up(m.drs), stream=stream)
+    bank = up(synth.logit_bank(cfg["n_exp"], 64, cfg["seed"]))
+    xd, sgw = up(m.x), up(m.sgw)
+    sel = torch.empty(cfg["top_k"] + 1, dtype=torch.int32, device=dev)
+    wsel = torch.empty(cfg["top_k"] + 1, device=dev)
+    outv = torch.empty(cfg["hidden"], device=dev)
+
+    def moe_step(i):
+        qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xd, sel=sel, w=wsel,
+                            stream=stream)
+        qmv.moe_ffn_q8row(gate, upw, down, sel, wsel, xd, outv, stream=stream)
+
+    t = kernel_time(moe_step, 64, stream)
+    ts = kernel_time(lambda i: qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xd,
+                                                    sel=sel, w=wsel, stream=stream), 64, stream)
+    b = moe_bytes(cfg["top_k"] + 1, cfg["hidden"], cfg["inter"])
+    out["moe_decode_h2048_e128_k8"] = {"kernels": "moe_select_kernel, moe_gate_up_kernel, moe_down_kernel",
+                                       "us_per_step": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                                       "frac_hbm": round(b / t / 1e9 / hbm, 4), "bytes": b,
+                                       "select_us": round(ts * 1e6, 3),
+                                       "l2": "64 rotated logit vectors over a 609 MB expert pool"}
+    for w_ in (gate, upw, down):
+        w_.free()
+    return out
+
+
+def cpu_baseline(oracle, host, min_seconds: float):
+    """The oracle as it stands, on all host cores, over the full workload
+    (both layouts), repeated until at least `min_seconds` have passed."""
+    threads = oracle.threads(0)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        for group in (64, 128):
+            codes, d, x = host[group]
+            oracle.q2(codes, d, group, x, nthreads=0)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    return {"value": round(STEP_BYTES * reps / el / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"{reps} full passes of q2 g64 + g128 17408x5120 (fp64 C oracle, {threads} threads)"}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    import oracle
+    from gemm_decode_prefill_gb300 import synth
+    if rank != 0:
+        return None
+    seed = synth.WORKLOADS["q2_gemv_17408x5120"]["seed"]
+    host = {g: synth.q2_inputs(Q2_ROWS, Q2_COLS, g, seed) for g in (64, 128)}
+    threads = oracle.threads(0)
+    # calibrate: seconds per row for both layouts
+    t0 = time.perf_counter()
+    probe = 1024
+    for g in (64, 128):
+        c, d, x = host[g]
+        oracle.q2(c[:probe], d[:probe], g, x)
+    per_row = (time.perf_counter() - t0) / probe
+    budget = float(args.ref_seconds)
+    rows = int(max(16, min(Q2_ROWS, budget / max(args.steps + args.warmup, 1) / max(per_row, 1e-9))))
+    for i in range(args.warmup):
+        for g in (64, 128):
+            c, d, x = host[g]
+            oracle.q2(c[:rows], d[:rows], g, x)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows) % (Q2_ROWS - rows + 1)
+        for g in (64, 128):
+            c, d, x = host[g]
+            oracle.q2(c[r0:r0 + rows], d[r0:r0 + rows], g, x)
+    el = time.perf_counter() - t0
+    frac = rows / Q2_ROWS
+    step_bytes = STEP_BYTES * frac
+    v = step_bytes * args.steps / el / 1e9
+    sample = f"{rows} of {Q2_ROWS} rows per step (g64 + g128), fp64 C oracle, {threads} threads"
+    return {"metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "q2_gemv_17408x5120_g64+g128", "rows": Q2_ROWS, "cols": Q2_COLS,
+                       "groups": [64, 128], "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "impl": "reference"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        line = run_reference(args, rank, world)
+    else:
+        rank, world, local = dist_setup()
+        line = run_ours(args, rank, world, local)
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -17,6 +17,7 @@
 // the row dot with act, scales by rs and the router weight, and the shares
 // are reduced in shared memory in a fixed order.
 #include <cfloat>
+#include <climits>
 
 #include "q8_block.cuh"
 
@@ -104,15 +105,35 @@ __global__ void __launch_bounds__(kSelThreads) moe_select_kernel(
     float mx = s_a[0];
     for (int w = 1; w < nw; ++w) mx = fmaxf(mx, s_a[w]);
     __syncthreads();
-    float es = 0.f;
+    // softmax denominator: compensated (TwoSum) summation, so its error is
+    // ~1 ulp however many logits there are
+    float es = 0.f, ec = 0.f;
 #pragma unroll
     for (int j = 0; j < kSelMaxPerThread; ++j)
-        if (live[j]) es += expf(v[j] - mx);
-    for (int off = 16; off > 0; off >>= 1) es += __shfl_xor_sync(0xffffffffu, es, off);
-    if (lane == 0) s_b[wid] = es;
+        if (live[j]) {
+            float t, e;
+            two_sum(es, expf(v[j] - mx), t, e);
+            es = t;
+            ec += e;
+        }
+    for (int off = 16; off > 0; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, es, off);
+        const float co = __shfl_xor_sync(0xffffffffu, ec, off);
+        float t, e;
+        two_sum(es, so, t, e);
+        es = t;
+        ec += co + e;
+    }
+    if (lane == 0) { s_a[wid] = es; s_b[wid] = ec; }
     __syncthreads();
-    float den = 0.f;
-    for (int w = 0; w < nw; ++w) den += s_b[w];
+    float den_s = s_a[0], den_c = s_b[0];
+    for (int w = 1; w < nw; ++w) {
+        float t, e;
+        two_sum(den_s, s_a[w], t, e);
+        den_s = t;
+        den_c += s_b[w] + e;
+    }
+    const float den = den_s + den_c;
 
     // ---- k rounds of block argmax over the unchosen logits ----
     bool chosen[kSelMaxPerThread] = {false, false, false, false};
@@ -145,7 +166,7 @@ __global__ void __launch_bounds__(kSelThreads) moe_select_kernel(
                 }
             s_pick = fi;
             sel[s] = fi;
-            s_wsel[s] = expf(fv - mx) / den;
+            s_wsel[s] = expf(fv - mx);   // unnormalised; divided below
         }
         __syncthreads();
         const int pick = s_pick;
@@ -155,9 +176,17 @@ __global__ void __launch_bounds__(kSelThreads) moe_select_kernel(
     }
 
     if (tid == 0) {
-        float wsum = 0.f;
-        for (int s = 0; s < k; ++s) wsum += s_wsel[s];
-        for (int s = 0; s < k; ++s) wout[s] = renorm ? s_wsel[s] / wsum : s_wsel[s];
+        // renormalised weights are e_s / sum_selected e (the softmax
+        // denominator cancels); the selected sum is compensated as well
+        float ws = 0.f, wc = 0.f;
+        for (int s = 0; s < k; ++s) {
+            float t, e;
+            two_sum(ws, s_wsel[s], t, e);
+            ws = t;
+            wc += e;
+        }
+        const float norm = renorm ? ws + wc : den;
+        for (int s = 0; s < k; ++s) wout[s] = s_wsel[s] / norm;
         if (sgw || sg_logit) {
             sel[k] = n;
             wout[k] = 1.0f / (1.0f + expf(-s_gate));
