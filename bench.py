@@ -240,10 +240,11 @@ def time_graph(g, replays: int, stream) -> float:
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    s.record(stream)
-    for _ in range(replays):
-        g.replay()
-    e.record(stream)
+    with torch.cuda.stream(stream):      # replay() launches on the current stream
+        s.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e.record(stream)
     torch.cuda.synchronize()
     return s.elapsed_time(e) / 1e3
 
@@ -281,16 +282,18 @@ def run_ours(args, rank, world, local):
         c_dev, d_dev = up(codes), up(d.view(np.int16))
         for _ in range(Q2_COPIES):
             W[group].append(qmv.qmv_pack_q2(c_dev, d_dev, group, stream=stream))
+        torch.cuda.synchronize()   # the packs read c_dev / d_dev asynchronously
         del c_dev, d_dev
-    x_dev = up(host[64][2])
+    # each layout is drawn from the workload seed with its own activation vector
+    xv = {group: up(host[group][2]) for group in (64, 128)}
     y64 = torch.empty(Q2_ROWS, device=dev)
     y128 = torch.empty(Q2_ROWS, device=dev)
     torch.cuda.synchronize()
 
     def step(i):
         c = i % Q2_COPIES
-        qmv.qmv_q2g64(W[64][c], x_dev, y64, stream=stream)
-        qmv.qmv_q2g128(W[128][c], x_dev, y128, stream=stream)
+        qmv.qmv_q2g64(W[64][c], xv[64], y64, stream=stream)
+        qmv.qmv_q2g128(W[128][c], xv[128], y128, stream=stream)
 
     # parity spot check of the benchmarked configuration (full outputs)
     with torch.cuda.stream(stream):
@@ -317,23 +320,23 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(replays):
-        g.replay()
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(stream):      # replay() launches on the current stream
+        s.record(stream)
+        for _ in range(replays):
+            g.replay()
         for i in range(rem):
             step(i)
-    e.record(stream)
+        e.record(stream)
     torch.cuda.synchronize()
     barrier()
     elapsed = s.elapsed_time(e) / 1e3
 
     # --- per-kernel roofline (each Q2 kernel alone, same rotation) ---
     def only64(i):
-        qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y64, stream=stream)
+        qmv.qmv_q2g64(W[64][i % Q2_COPIES], xv[64], y64, stream=stream)
 
     def only128(i):
-        qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y128, stream=stream)
+        qmv.qmv_q2g128(W[128][i % Q2_COPIES], xv[128], y128, stream=stream)
 
     t64 = kernel_time(only64, gsteps, stream, min_seconds=1.0)
     t128 = kernel_time(only128, gsteps, stream, min_seconds=1.0)
@@ -398,16 +401,16 @@ def run_e2e(args, qmv, W, host, dev, stream):
     """The same metric through the public API, host buffers in and out: per
     step the pinned host x goes to the device, both GEMVs run, both y come back."""
     import torch
-    x_host = torch.from_numpy(host[64][2].copy()).pin_memory()
+    x_host = torch.from_numpy(np.stack([host[64][2], host[128][2]])).pin_memory()
     y_host = torch.empty(2, Q2_ROWS, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty(Q2_COLS, device=dev)
+    x_dev = torch.empty(2, Q2_COLS, device=dev)
     y_dev = torch.empty(2, Q2_ROWS, device=dev)
     n = max(50, min(args.steps, 2000))
     for i in range(5):
         with torch.cuda.stream(stream):
             x_dev.copy_(x_host, non_blocking=True)
-            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y_dev[0], stream=stream)
-            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y_dev[1], stream=stream)
+            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev[0], y_dev[0], stream=stream)
+            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev[1], y_dev[1], stream=stream)
             y_host.copy_(y_dev, non_blocking=True)
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
@@ -418,14 +421,14 @@ def run_e2e(args, qmv, W, host, dev, stream):
     with torch.cuda.stream(stream):
         for i in range(n):
             x_dev.copy_(x_host, non_blocking=True)
-            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev, y_dev[0], stream=stream)
-            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev, y_dev[1], stream=stream)
+            qmv.qmv_q2g64(W[64][i % Q2_COPIES], x_dev[0], y_dev[0], stream=stream)
+            qmv.qmv_q2g128(W[128][i % Q2_COPIES], x_dev[1], y_dev[1], stream=stream)
             y_host.copy_(y_dev, non_blocking=True)
     e.record(stream)
     torch.cuda.synchronize()
     t = s.elapsed_time(e) / 1e3
     v, _ = aggregate(t, STEP_BYTES * n / 1e9, int(os.environ.get("WORLD_SIZE", "1")))
-    return {"value": round(v, 1), "unit": "GB/s", "steps": n, "h2d_bytes_per_step": Q2_COLS * 4,
+    return {"value": round(v, 1), "unit": "GB/s", "steps": n, "h2d_bytes_per_step": 2 * Q2_COLS * 4,
             "d2h_bytes_per_step": 2 * Q2_ROWS * 4, "path": "qmv.qmv_q2g64 + qmv.qmv_q2g128 (C ABI), eager"}
 
 
@@ -439,6 +442,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
     qd, rd = up(q), up(rs)
     ws = [qmv.qmv_pack_q8row(qd, rd, stream=stream) for _ in range(16)]
+    torch.cuda.synchronize()
     xd = up(xs)
     y = torch.empty(cfg["rows"], device=dev)
     t = kernel_time(lambda i: qmv.qmv_q8row(ws[i % 16], xd, y, stream=stream), 160, stream)
@@ -453,6 +457,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     cfg = synth.WORKLOADS["q8_lm_head_151936x4096"]
     q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
     w = qmv.qmv_pack_q8row(up(q), up(rs), stream=stream)
+    torch.cuda.synchronize()
     del q
     xd = up(xs)
     y = torch.empty(cfg["rows"], device=dev)
@@ -468,6 +473,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     q, rs, xs = synth.qmm_inputs(cfg["rows"], cfg["cols"], cfg["nb"], cfg["seed"])
     qd, rd = up(q), up(rs)
     ws = [qmv.qmv_pack_q8row(qd, rd, stream=stream) for _ in range(4)]
+    torch.cuda.synchronize()
     del qd, rd
     xd = up(xs)
     y = torch.empty(cfg["nb"], cfg["rows"], device=dev)
@@ -488,6 +494,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     gate = qmv.qmv_pack_q8row(up(m.gq), up(m.grs), stream=stream)
     upw = qmv.qmv_pack_q8row(up(m.uq), up(m.urs), stream=stream)
     down = qmv.qmv_pack_q8row(up(m.dq), up(m.drs), stream=stream)
+    torch.cuda.synchronize()
     bank = up(synth.logit_bank(cfg["n_exp"], 64, cfg["seed"]))
     xd, sgw = up(m.x), up(m.sgw)
     sel = torch.empty(cfg["top_k"] + 1, dtype=torch.int32, device=dev)
