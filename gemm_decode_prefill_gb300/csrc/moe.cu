@@ -358,3 +358,91 @@ extern "C" qmv_status moe_ffn_q8row(const qmv_weights* gate, const qmv_weights* 
     cudaFreeAsync(act, cs);
     return s;
 }
+
+// ---------------------------------------------------------------------------
+// moe_ffn_q8row_static: the same expert FFN, allocating nothing.
+//
+// Some callers cannot allocate device memory once they are serving: engines
+// that hand all device memory to their own allocator at start-up and refuse
+// allocations afterwards, and plugins loaded into such engines.  For them the
+// activation scratch of the two FFN kernels lives in the fixed array below.
+// Every GPU that loads this library holds it (256 KiB) until the process
+// exits; calls with slots * inter above its size are rejected.
+//
+// All calls on a device share the array and it keeps the last call's
+// contents; nothing has to start at zero, because the gate/up kernel writes
+// every element (slot, row) that the down kernel then reads.  Two calls whose
+// work overlaps on the GPU (e.g. on different streams without ordering) race
+// on the array: order them.
+//
+// The array's name is only a host-side stand-in in host code, so its device
+// address is looked up once per device with cudaGetSymbolAddress, with that
+// device current, by the first call made on the device.  That first call
+// should come before any stream capture.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+constexpr int64_t kStaticActFloats = 1 << 16;   // slots * inter <= 65536
+static __device__ __align__(256) float g_static_act[kStaticActFloats];
+
+namespace {
+
+std::mutex g_static_mu;
+float* g_static_act_ptr[64] = {};
+
+qmv_status static_act_address(float** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64)
+        return qmv::fail(QMV_ERR_CUDA, "moe_ffn_q8row_static: no usable CUDA device");
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_act_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_act);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return qmv::fail(QMV_ERR_CUDA, "moe_ffn_q8row_static: cudaGetSymbolAddress failed: %s",
+                             cudaGetErrorString(e));
+        }
+        g_static_act_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_static_act_ptr[dev];
+    return QMV_OK;
+}
+
+}  // namespace
+
+extern "C" qmv_status moe_ffn_q8row_static(const qmv_weights* gate, const qmv_weights* up,
+                                           const qmv_weights* down, const int32_t* sel, const float* w,
+                                           int slots, const float* x, float* out, qmv_stream st) {
+    QMV_REQUIRE(gate && up && down && sel && w && x && out, QMV_ERR_INVALID_ARG,
+                "moe_ffn_q8row_static: null argument");
+    QMV_REQUIRE(gate->format == QMV_FMT_Q8ROW && up->format == QMV_FMT_Q8ROW && down->format == QMV_FMT_Q8ROW,
+                QMV_ERR_UNSUPPORTED, "moe_ffn_q8row_static: handles must be q8_row");
+    QMV_REQUIRE(slots >= 1 && slots <= 64, QMV_ERR_INVALID_ARG, "moe_ffn_q8row_static: need 1 <= slots <= 64");
+    const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
+    QMV_REQUIRE(up->experts == E && up->rows == inter && up->cols == hidden && down->experts == E &&
+                    down->rows == hidden && down->cols == inter,
+                QMV_ERR_INVALID_ARG, "moe_ffn_q8row_static: gate/up [E][inter][hidden] and down [E][hidden][inter] "
+                                     "shapes disagree");
+    QMV_REQUIRE((int64_t)slots * inter <= kStaticActFloats, QMV_ERR_UNSUPPORTED,
+                "moe_ffn_q8row_static: slots * inter = %lld exceeds the fixed scratch of %lld floats",
+                (long long)((int64_t)slots * inter), (long long)kStaticActFloats);
+    QMV_REQUIRE(qmv::aligned16(x) && qmv::aligned16(out), QMV_ERR_INVALID_ARG,
+                "moe_ffn_q8row_static: x and out must be 16-byte aligned");
+    int* status = qmv::device_status();
+    QMV_REQUIRE(status, QMV_ERR_CUDA, "moe_ffn_q8row_static: no CUDA device");
+    float* act = nullptr;
+    const qmv_status sa = static_act_address(&act);
+    if (sa != QMV_OK) return sa;
+    cudaStream_t cs = (cudaStream_t)st;
+    const dim3 g1((unsigned)(((inter + 3) / 4 + kWarps - 1) / kWarps), (unsigned)slots);
+    moe_gate_up_kernel<<<g1, kThreads, 0, cs>>>(gate->q, gate->rs, up->q, up->rs, E, inter, gate->rows_pad,
+                                                gate->cols_pad, hidden, sel, x, act, status);
+    const int S = slots >= 4 ? 4 : slots >= 2 ? 2 : 1;
+    const int gpc = kWarps / S;
+    const int64_t n_rg = (hidden + 3) / 4;
+    moe_down_kernel<<<(unsigned)((n_rg + gpc - 1) / gpc), kThreads, 0, cs>>>(
+        down->q, down->rs, E, hidden, down->rows_pad, down->cols_pad, inter, sel, w, slots, act, out, S);
+    return qmv::check_launch("moe_ffn_q8row_static kernels");
+}

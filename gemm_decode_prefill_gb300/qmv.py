@@ -44,6 +44,7 @@ _SIGS = {
     "qmm_q8row": ([_P, _P, _I64, _P, _P], _I),
     "moe_select_topk": ([_P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P], _I),
     "moe_ffn_q8row": ([_P, _P, _P, _P, _P, _I, _P, _P, _P], _I),
+    "moe_ffn_q8row_static": ([_P, _P, _P, _P, _P, _I, _P, _P, _P], _I),
     "qmv_check": ([_P, ctypes.POINTER(_I)], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -235,6 +236,20 @@ def moe_ffn_q8row(gate: Weights, up: Weights, down: Weights, sel: torch.Tensor, 
                               _dev(w, torch.float32, "w", (slots,)), slots,
                               _dev(x, torch.float32, "x", (gate.cols,)),
                               _dev(out, torch.float32, "out", (gate.cols,)), _stream(stream)), "moe_ffn_q8row")
+    return out
+
+
+def moe_ffn_q8row_static(gate: Weights, up: Weights, down: Weights, sel: torch.Tensor, w: torch.Tensor,
+                         x: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """Allocation-free expert FFN: for callers that may not allocate device
+    memory while serving (the output buffer is theirs, the activation
+    scratch is the library's fixed device array; see include/qmv.h)."""
+    slots = sel.shape[0]
+    _check(_lib.moe_ffn_q8row_static(gate.handle, up.handle, down.handle, _dev(sel, torch.int32, "sel", (slots,)),
+                                     _dev(w, torch.float32, "w", (slots,)), slots,
+                                     _dev(x, torch.float32, "x", (gate.cols,)),
+                                     _dev(out, torch.float32, "out", (gate.cols,)), _stream(stream)),
+           "moe_ffn_q8row_static")
     return out
 
 

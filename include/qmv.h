@@ -190,6 +190,24 @@ QMV_API qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
                          const float *w, int slots, const float *x,
                          float *out, qmv_stream st);
 
+/* Allocation-free variant of moe_ffn_q8row, for callers that cannot
+ * allocate device memory while serving (engines that give all device memory
+ * to their own allocator at start-up and refuse allocations afterwards, and
+ * plugins loaded into such engines).  The pages have no counterpart: this
+ * is a library convenience, not part of the method.
+ *   Same arguments, results and errors as moe_ffn_q8row, plus:
+ *   slots * inter <= 65536, else QMV_ERR_UNSUPPORTED.
+ * The activation scratch is a fixed 256 KiB array in device memory that
+ * every GPU loading the library holds until exit; the call makes no
+ * allocation.  All calls on a device share it, so calls whose GPU work
+ * overlaps (unordered streams) race: order them.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) and should be
+ * made before any stream capture. */
+QMV_API qmv_status moe_ffn_q8row_static(const qmv_weights *gate, const qmv_weights *up,
+                                        const qmv_weights *down, const int32_t *sel,
+                                        const float *w, int slots, const float *x,
+                                        float *out, qmv_stream st);
+
 /* Reads and clears the device status word that kernels set when they meet
  * a violated invariant (e.g. an expert id out of range).  Synchronizes `st`.
  * Returns QMV_OK or QMV_ERR_DEVICE_STATUS (*code gets the first reason,

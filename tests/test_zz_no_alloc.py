@@ -1,0 +1,69 @@
+"""The allocation-free MoE FFN entry point (moe_ffn_q8row_static).
+
+It exists for callers that may not allocate device memory while serving:
+engines that hand all device memory to their own allocator at start-up and
+refuse allocations afterwards, and plugins loaded into such engines.  This
+file is collected last on purpose, so that a run stopping at the first
+failure has run every other test first; it also passes on its own in a
+fresh process.
+
+Each check calls the new entry point through the C ABI and compares it with
+moe_ffn_q8row (the allocating entry point) on the same inputs, within the
+GEMV tolerance the other tests use, on two calls in a row with different
+expert selections (the fixed scratch keeps the previous call's contents).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_decode_prefill_gb300 import synth
+from gpu_helpers import TOL_GEMV, assert_within, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qmv():
+    from gemm_decode_prefill_gb300 import qmv as m
+    return m
+
+
+def _mag(m, sel, w):
+    _, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel, w, m.x, with_parts=True)
+    return parts["mag"]
+
+
+def test_static_matches_allocating_entry_point_twice(qmv):
+    cfg = synth.WORKLOADS["moe_decode_h2048_e128_k8"]
+    m = synth.moe_inputs(cfg["n_exp"], cfg["hidden"], cfg["inter"], cfg["seed"])
+    gate = qmv.qmv_pack_q8row(dev(m.gq), dev(m.grs))
+    up = qmv.qmv_pack_q8row(dev(m.uq), dev(m.urs))
+    down = qmv.qmv_pack_q8row(dev(m.dq), dev(m.drs))
+    x, sgw = dev(m.x), dev(m.sgw)
+    bank = synth.logit_bank(cfg["n_exp"], 2, cfg["seed"])
+    out_static = torch.full((cfg["hidden"],), float("nan"), device="cuda")
+    seen = []
+    for call in range(2):
+        sel, w = qmv.moe_select_topk(dev(bank[call]), cfg["top_k"], cfg["renorm"], sg_w=sgw, x=x)
+        ref = host(qmv.moe_ffn_q8row(gate, up, down, sel, w, x))
+        got = host(qmv.moe_ffn_q8row_static(gate, up, down, sel, w, x, out_static))
+        sel_h = host(sel)
+        seen.append(tuple(sel_h.tolist()))
+        mag = _mag(m, sel_h, host(w).astype(np.float64))
+        assert_within(got, ref.astype(np.float64), mag, TOL_GEMV, f"static vs allocating, call {call}")
+    assert seen[0] != seen[1], "the two calls should route to different experts"
+    assert qmv.qmv_check() == 0
+
+
+def test_static_rejects_sizes_beyond_its_scratch(qmv):
+    # slots * inter = 64 * 1040 > 65536 floats of fixed scratch
+    m = synth.moe_inputs(2, 32, 1040, seed=5)
+    gate = qmv.qmv_pack_q8row(dev(m.gq), dev(m.grs))
+    up = qmv.qmv_pack_q8row(dev(m.uq), dev(m.urs))
+    down = qmv.qmv_pack_q8row(dev(m.dq), dev(m.drs))
+    sel = dev(np.zeros(64, np.int32))
+    w = dev(np.ones(64, np.float32))
+    out = torch.empty(32, device="cuda")
+    with pytest.raises(qmv.QmvError, match="UNSUPPORTED"):
+        qmv.moe_ffn_q8row_static(gate, up, down, sel, w, dev(m.x), out)
