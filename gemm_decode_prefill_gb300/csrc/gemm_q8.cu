@@ -26,7 +26,7 @@
 
 #include <mutex>
 
-#include "qmv_internal.cuh"
+#include "tma_util.cuh"
 
 namespace {
 
@@ -36,8 +36,6 @@ constexpr int kABytes = BM * BK * 2;     // bf16 A tile
 constexpr int kBBytes = BN * BK * 2;     // bf16 B tile
 constexpr int kThreads = 384;
 constexpr int kTmemCols = 512;           // two 256-column accumulators
-constexpr uint32_t kSpinFast = 4096;
-constexpr uint32_t kSpinLimit = 1u << 22;  // ~1 s with the backoff below
 
 struct __align__(1024) Smem {
     uint8_t b[STAGES][kBBytes];
@@ -52,50 +50,13 @@ struct __align__(1024) Smem {
     int abort;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
+using qmv::smem_u32;
+using qmv::mbar_init;
+using qmv::mbar_arrive_tx;
+using qmv::mbar_arrive;
+using qmv::mbar_wait;
+using qmv::fence_proxy_async_smem;
 
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with parity `parity`.  Returns false if the
-// kernel is aborting (this wait expired, or another role's did).
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort, int* status) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try(b, parity)) return true;
-        if (i >= kSpinFast) {
-            if (*abort) return false;
-            __nanosleep(256);
-        }
-    }
-    *abort = 1;
-    atomicCAS(status, 0, qmv::kDevTimeout);
-    return false;
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

@@ -64,7 +64,8 @@ def test_q8row_is_deterministic_and_does_not_write_outside(qmv):
 
 # --------------------------------------------------------------------- Q2
 
-Q2_SHAPES = [(1, 128), (17, 128), (33, 192), (100, 640), (257, 1024), (1000, 5120)]
+Q2_SHAPES = [(1, 128), (17, 128), (33, 192), (100, 640), (257, 1024), (1000, 5120), (47, 8192),
+             (40, 16384), (64, 20480), (4096, 4096)]
 
 
 @pytest.mark.parametrize("group", [64, 128])
