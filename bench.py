@@ -157,7 +157,9 @@ def source_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-Q2_SOURCES = ["gemm_decode_prefill_gb300/csrc/gemv_q2.cu", "gemm_decode_prefill_gb300/csrc/qmv_internal.cuh"]
+Q2_SOURCES = ["gemm_decode_prefill_gb300/csrc/gemv_q2.cu", "gemm_decode_prefill_gb300/csrc/qmv_internal.cuh",
+              "gemm_decode_prefill_gb300/csrc/tma_util.cuh"]
+Q2_KERNEL = "q2_gemv_v3_kernel<{g}>"   # the kernel the 17408 x 5120 workload dispatches to
 
 
 def recorded_traffic(kernel_tag: str, digest: str):
@@ -347,11 +349,11 @@ def run_ours(args, rank, world, local):
     tdom = t64 if dom == 64 else t128
     ach = q2_bytes(Q2_ROWS, Q2_COLS, dom) / tdom / 1e9
     digest = source_digest(Q2_SOURCES)
-    roofline = {"bound": "hbm", "kernel": f"q2_gemv_kernel<{dom}>", "achieved": round(ach, 1),
+    roofline = {"bound": "hbm", "kernel": Q2_KERNEL.format(g=dom), "achieved": round(ach, 1),
                 "peak": peaks["hbm_gbs"], "peak_source": peaks["source"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm_gbs"], 4),
-                "traffic": recorded_traffic(f"q2_gemv_kernel<{dom}>", digest),
-                "other": {"kernel": f"q2_gemv_kernel<{192 - dom}>",
+                "traffic": recorded_traffic(Q2_KERNEL.format(g=dom), digest),
+                "other": {"kernel": Q2_KERNEL.format(g=192 - dom),
                           "achieved": round(q2_bytes(Q2_ROWS, Q2_COLS, 192 - dom) / (t128 if dom == 64 else t64) / 1e9, 1)},
                 "source_digest": digest}
 
