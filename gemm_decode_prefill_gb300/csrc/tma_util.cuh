@@ -8,9 +8,6 @@
 
 namespace qmv {
 
-constexpr uint32_t kSpinFast = 4096;
-constexpr uint32_t kSpinLimit = 1u << 22;  // ~1 s with the back-off below
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -40,17 +37,50 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in the barrier unit until completion or ~`ns` nanoseconds, instead of
+// re-issuing probes that slow every other barrier operation on the SM.
+__device__ __forceinline__ bool mbar_try_sleep(uint64_t* b, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+constexpr uint64_t kWaitNs = 1000000000ull;   // a wait gives up after 1 s
+
 // Bounded wait for the phase with parity `parity`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort, int* status) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (mbar_try(b, parity)) return true;
-        if (i >= kSpinFast) {
-            if (*abort) return false;
-            __nanosleep(256);
-        }
-    }
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    do {
+        if (mbar_try_sleep(b, parity, 1000)) return true;
+        if (*abort) return false;
+    } while (global_ns() - t0 < kWaitNs);
     *abort = 1;
     atomicCAS(status, 0, kDevTimeout);
+    return false;
+}
+
+// Bounded wait that ignores the abort flag: lets copies or MMAs that were
+// already issued land before the CTA releases its shared or tensor memory.
+__device__ __forceinline__ bool mbar_drain(uint64_t* b, uint32_t parity) {
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = global_ns();
+    do {
+        if (mbar_try_sleep(b, parity, 1000)) return true;
+    } while (global_ns() - t0 < kWaitNs);
     return false;
 }
 
@@ -71,6 +101,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Named barrier over `nthreads` threads (id 1..15; id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Launches `kernel` as a programmatic dependent launch: it may start while
+// the previous kernel in the stream is still running, and must execute
+// griddepcontrol.wait before it reads anything that kernel may produce.
+template <typename... KArgs, typename... Args>
+qmv_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QMV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return QMV_OK;
 }
 
 }  // namespace qmv

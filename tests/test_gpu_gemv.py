@@ -65,7 +65,7 @@ def test_q8row_is_deterministic_and_does_not_write_outside(qmv):
 # --------------------------------------------------------------------- Q2
 
 Q2_SHAPES = [(1, 128), (17, 128), (33, 192), (100, 640), (257, 1024), (1000, 5120), (47, 8192),
-             (40, 16384), (64, 20480), (4096, 4096)]
+             (40, 16384), (64, 20480), (4096, 4096), (3, 1920), (2, 32768), (1200, 384)]
 
 
 @pytest.mark.parametrize("group", [64, 128])
@@ -138,3 +138,55 @@ def test_q2_wrong_group_entry_point_is_rejected(qmv):
     w8 = qmv.qmv_pack_q8row(dev(q8), dev(rs))
     with pytest.raises(qmv.QmvError, match="UNSUPPORTED"):
         qmv.qmv_q2g64(w8, dev(x))
+
+
+def test_q2_too_wide_is_rejected(qmv):
+    cols = (1 << 24) + 128
+    codes = torch.zeros((1, cols // 4), dtype=torch.uint8, device="cuda")
+    d = torch.zeros((1, cols // 128), dtype=torch.int16, device="cuda")
+    with pytest.raises(qmv.QmvError, match="UNSUPPORTED"):
+        qmv.qmv_pack_q2(codes, d, 128)
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_all_zero_weights_give_exact_zero(qmv, group):
+    """Code 1 is the weight 0: the tensor-core path must give exactly 0, not
+    a cancellation residue, for any x."""
+    rows, cols = 300, 2048
+    codes = np.full((rows, cols // 4), 0x55, np.uint8)
+    d = np.full((rows, cols // group), 0x3C00, np.uint16)   # d = 1
+    x = synth.rng(58).standard_normal(cols).astype(np.float32) * 1e3
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+    fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+    assert np.array_equal(host(fn(w, dev(x))), np.zeros(rows, np.float32))
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1.0, 1e6, 1e30])
+def test_q2_activation_magnitudes(qmv, scale):
+    """The split of x into e4m3 parts follows max|x|: results stay inside the
+    bound across 60 decades of activation size and with a wide dynamic range
+    inside one vector."""
+    rows, cols = 520, 1024
+    codes, d, x = synth.q2_inputs(rows, cols, 64, seed=59)
+    x = (x * scale).astype(np.float32)
+    x[::7] *= np.float32(1e-3)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), 64)
+    y = host(qmv.qmv_q2g64(w, dev(x)))
+    y_ref, mag = oracle.q2(codes, d, 64, x, with_mag=True)
+    assert_within(y, y_ref, mag, TOL_GEMV, f"q2 |x| ~ {scale}")
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_repeated_calls_are_identical(qmv, group):
+    """Back-to-back calls on the full workload: any race between the kernel's
+    pipeline stages shows up as tiles that differ between calls."""
+    cfg = synth.WORKLOADS["q2_gemv_17408x5120"]
+    codes, d, x = synth.q2_inputs(cfg["rows"], cfg["cols"], group, cfg["seed"] + 7)
+    w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+    fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+    xd = dev(x)
+    ys = [host(fn(w, xd)) for _ in range(3)]
+    y_ref, mag = oracle.q2(codes, d, group, x, with_mag=True)
+    for y in ys:
+        assert_within(y, y_ref, mag, TOL_GEMV, f"q2 g{group} repeated")
+    assert all(np.array_equal(ys[0], y) for y in ys[1:])
