@@ -449,7 +449,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     y = torch.empty(cfg["rows"], device=dev)
     t = kernel_time(lambda i: qmv.qmv_q8row(ws[i % 16], xd, y, stream=stream), 160, stream)
     b = q8_bytes(cfg["rows"], cfg["cols"])
-    out["q8_gemv_4096x4096"] = {"kernel": "q8row_gemv_kernel", "us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+    out["q8_gemv_4096x4096"] = {"kernel": "q8row_gemv_smem_kernel", "us": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                                 "frac_hbm": round(b / t / 1e9 / hbm, 4), "bytes": b, "l2": "16 rotated copies"}
     for w_ in ws:
         w_.free()
@@ -512,7 +512,7 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     ts = kernel_time(lambda i: qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xd,
                                                     sel=sel, w=wsel, stream=stream), 64, stream)
     b = moe_bytes(cfg["top_k"] + 1, cfg["hidden"], cfg["inter"])
-    out["moe_decode_h2048_e128_k8"] = {"kernels": "moe_select_kernel, moe_gate_up_kernel, moe_down_kernel",
+    out["moe_decode_h2048_e128_k8"] = {"kernels": "moe_select_kernel, moe_gate_up_smem_kernel, moe_down_smem_kernel",
                                        "us_per_step": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                                        "frac_hbm": round(b / t / 1e9 / hbm, 4), "bytes": b,
                                        "select_us": round(ts * 1e6, 3),

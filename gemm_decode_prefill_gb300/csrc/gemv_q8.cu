@@ -9,7 +9,20 @@
 // is split across the warps of a CTA when the row count alone cannot fill
 // the GPU, and the S partial sums are reduced in shared memory in a fixed
 // order (deterministic).
+//
+// Two kernels.  q8row_gemv_smem_kernel (matrices of at most 2 x SMs x 96 KB
+// of codes, about 28 MB, whose 4-row group fits in 96 KB): a CTA owns a
+// contiguous run of row groups
+// (balanced over at least two CTAs per SM) and, before anything else, one
+// thread issues bulk copies of that whole run into shared memory.  The kernel
+// is a programmatic dependent launch, so those copies overlap the tail of the
+// previous kernel in the stream; only then does it wait for that kernel and
+// read xs.  The 8 warps split the CTA's (row group, 128-column block) pairs
+// evenly, and the per-warp partial sums of each row are added in warp order
+// (deterministic).  q8row_gemv_kernel (larger matrices) streams the codes
+// through registers instead, its first batch also loaded before the wait.
 #include "q8_block.cuh"
+#include "tma_util.cuh"
 
 namespace {
 
@@ -31,8 +44,13 @@ __global__ void __launch_bounds__(kThreads) q8row_gemv_kernel(
     const int64_t nblk = cols_pad / 128;
     const int64_t b0 = nblk * ks / S, b1 = nblk * (ks + 1) / S;
     const bool live = rg * 4 < rows;
+    // before the dependency wait: this warp's first codes (weights only)
+    uint4 w0[kUnroll];
+    qmv::q8_first_codes<kUnroll>(w0, q, cols_pad, rg, b0, live ? b1 : b0, lane);
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
     float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (live) qmv::q8_rowgroup_dot<kUnroll>(q, cols_pad, rg, b0, b1, xs, cols, lane, v);
+    if (live) qmv::q8_rowgroup_dot_from<kUnroll>(w0, q, cols_pad, rg, b0, b1, xs, cols, lane, v);
 #pragma unroll
     for (int r = 0; r < 4; ++r) v[r] = qmv::warp_sum(v[r]);
     if (S == 1) {
@@ -57,6 +75,93 @@ __global__ void __launch_bounds__(kThreads) q8row_gemv_kernel(
     }
 }
 
+constexpr int kMaxRG = 24;                       // row groups per CTA
+constexpr int64_t kSmemCodes = 96 * 1024;        // codes staged per CTA
+
+// CTA c: row groups [c * n_rg / G, (c + 1) * n_rg / G), at most kMaxRG and
+// kSmemCodes bytes of codes.
+__global__ void __launch_bounds__(kThreads) q8row_gemv_smem_kernel(
+    const int8_t* __restrict__ q, const float* __restrict__ rs, const float* __restrict__ xs,
+    float* __restrict__ y, int64_t rows, int64_t cols, int64_t cols_pad, int64_t n_rg, int64_t G, int* status) {
+    extern __shared__ __align__(128) uint8_t smc[];
+    __shared__ __align__(8) uint64_t bar[kMaxRG];
+    __shared__ float part[kMaxRG][kWarps][4];
+    __shared__ int abort_flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t g0 = (int64_t)blockIdx.x * n_rg / G, g1 = ((int64_t)blockIdx.x + 1) * n_rg / G;
+    const int R = (int)(g1 - g0);
+    const int64_t rgb = 4 * cols_pad;   // bytes of one row group
+    const int nblk = (int)(cols_pad / 128);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int r = 0; r < R; ++r) qmv::mbar_init(&bar[r], 1);
+        qmv::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // the codes are constant, so they may be fetched before the wait
+        for (int r = 0; r < R; ++r) {
+            qmv::mbar_arrive_tx(&bar[r], (uint32_t)rgb);
+            const int8_t* src = q + (g0 + r) * rgb;
+            for (int64_t o = 0; o < rgb; o += 32768)
+                qmv::bulk_g2s(smc + r * rgb + o, src + o, (uint32_t)(rgb - o < 32768 ? rgb - o : 32768), &bar[r]);
+        }
+    }
+    for (int i = threadIdx.x; i < R * kWarps * 4; i += kThreads) (&part[0][0][0])[i] = 0.f;
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+    __syncthreads();
+
+    // warp w: flattened (row group, block) pairs [w T / 8, (w + 1) T / 8)
+    const int T = R * nblk;
+    const int a = warp * T / kWarps, b = (warp + 1) * T / kWarps;
+    for (int i = a; i < b;) {
+        const int r = i / nblk;
+        const int bs = i - r * nblk;
+        const int be = (b - r * nblk) < nblk ? (b - r * nblk) : nblk;
+        if (!qmv::mbar_wait(&bar[r], 0, &abort_flag, status)) break;
+        const uint8_t* base = smc + r * rgb + lane * 16;
+        float2 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+        int blk = bs;
+        for (; blk + 4 <= be; blk += 4) {
+            uint4 wv[4];
+            float4 xv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) wv[u] = *reinterpret_cast<const uint4*>(base + (blk + u) * 512);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) xv[u] = qmv::act_for_block(xs, blk + u, lane, cols);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) qmv::q8_chunk_fma(wv[u], xv[u], acc);
+        }
+        for (; blk < be; ++blk)
+            qmv::q8_chunk_fma(*reinterpret_cast<const uint4*>(base + blk * 512), qmv::act_for_block(xs, blk, lane, cols),
+                              acc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float v = qmv::warp_sum(acc[k].x + acc[k].y);
+            if (lane == 0) part[r][warp][k] = v;
+        }
+        i = r * nblk + be;
+    }
+    __syncthreads();
+    if (abort_flag) {
+        // a wait gave up: let every copy land before the CTA's shared memory is released
+        if (threadIdx.x == 0)
+            for (int r = 0; r < R; ++r) qmv::mbar_drain(&bar[r], 0);
+        return;
+    }
+    for (int t = threadIdx.x; t < R * 4; t += kThreads) {
+        const int r = t >> 2, k = t & 3;
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += part[r][w][k];
+        const int64_t row = (g0 + r) * 4 + k;
+        if (row < rows) y[row] = rs[row] * s;
+    }
+}
+
 // Number of warps a row group's K range is split across: enough warps to
 // fill the GPU several times over, but at least 4 blocks of 128 columns each.
 int choose_split(int64_t n_rg, int64_t nblk) {
@@ -76,10 +181,32 @@ extern "C" qmv_status qmv_q8row(const qmv_weights* w, const float* xs, float* y,
                 "qmv_q8row: xs and y must be 16-byte aligned");
     const int64_t n_rg = (w->rows + 3) / 4;
     const int64_t nblk = w->cols_pad / 128;
+    const int64_t rgb = 4 * w->cols_pad;
+    cudaStream_t cs = (cudaStream_t)st;
+    // The staged kernel pays off while the whole matrix fits in one resident
+    // wave (two CTAs of kSmemCodes per SM), where loading before the
+    // dependency wait hides the launch gap; larger matrices stream through
+    // registers at a higher rate.
+    if (rgb <= kSmemCodes && w->rows_pad * w->cols_pad <= 2 * (int64_t)qmv::sm_count() * kSmemCodes) {
+        int* status = qmv::device_status();
+        QMV_REQUIRE(status, QMV_ERR_CUDA, "qmv_q8row: no CUDA device");
+        const int64_t rmax = kSmemCodes / rgb < kMaxRG ? kSmemCodes / rgb : kMaxRG;
+        int64_t G = 2 * (int64_t)qmv::sm_count();
+        if (G < (n_rg + rmax - 1) / rmax) G = (n_rg + rmax - 1) / rmax;
+        if (G > n_rg) G = n_rg;
+        const int64_t rcta = (n_rg + G - 1) / G;   // most row groups any CTA gets
+        static int configured[64] = {0};
+        const int dev = qmv::current_device();
+        if (dev >= 0 && dev < 64 && !configured[dev]) {
+            cudaFuncSetAttribute(q8row_gemv_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemCodes);
+            configured[dev] = 1;
+        }
+        return qmv::launch_pdl(q8row_gemv_smem_kernel, dim3((unsigned)G), dim3(kThreads), (size_t)(rcta * rgb), cs,
+                               w->q, w->rs, xs, y, w->rows, w->cols, w->cols_pad, n_rg, G, status);
+    }
     const int S = choose_split(n_rg, nblk);
     const int gpc = kWarps / S;
     const int64_t grid = (n_rg + gpc - 1) / gpc;
-    q8row_gemv_kernel<<<(unsigned)grid, kThreads, 0, (cudaStream_t)st>>>(
-        w->q, w->rs, xs, y, w->rows, w->cols, w->cols_pad, S);
-    return qmv::check_launch("q8row_gemv_kernel");
+    return qmv::launch_pdl(q8row_gemv_kernel, dim3((unsigned)grid), dim3(kThreads), 0, cs, w->q, w->rs, xs, y,
+                           w->rows, w->cols, w->cols_pad, S);
 }

@@ -1,30 +1,48 @@
 // MoE decode step: router select and the expert FFN over the selected slots.
 //
 // Router select (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_select_sg`
-// and `moe_select`): one CTA, all-parallel.  The shared-expert gate dot is
+// and `moe_select`): one CTA.  Warp 0 holds the logits in registers and runs
+// the top_k rounds of argmax: per round every lane takes its best unchosen
+// logit, the warp takes the largest order-preserving integer key of those
+// values (redux.sync max) and, among the lanes holding that key, the lowest
+// expert index (redux.sync min).  So equal values go to the lowest index,
+// +0 and -0 compare equal, and chosen experts are excluded by index (their
+// key is cleared), never by overwriting a logit: every finite logit is
+// handled.  Meanwhile warps 1..7 form the shared-expert gate dot,
 // compensated (Ogita-Rump-Oishi Dot2: TwoProduct via FMA + TwoSum), so the
-// sigmoid weight stays within 1e-6 relative of the exact value; the softmax
-// max and denominator are block reductions; the top-k is k rounds of a
-// block argmax on the raw f32 logits with the lowest index winning equal
-// values, and chosen experts are excluded by a flag (not by overwriting the
-// logit with a sentinel), so every finite logit is handled.
+// sigmoid weight stays within 1e-6 relative of the exact value.  The top-1
+// logit is the softmax maximum; the softmax denominator and the selected
+// sum are TwoSum-compensated.
 //
 // Expert FFN (cortiq-engine 0.5.43 src/gpu_wgpu.rs, WGSL `moe_gate_up` and
 // `moe_down`; cortiq-engine 0.3.7 src/gpu_metal.rs, host `moe_block`): two
-// kernels.  gate/up: a warp owns a 4-row group of BOTH matrices of one slot
-// (they share the x reads) and writes act = silu(g) * u.  down: a warp owns
-// a 4-row group of the output and a share of the slots; per slot it forms
-// the row dot with act, scales by rs and the router weight, and the shares
-// are reduced in shared memory in a fixed order.
-#include <cfloat>
-#include <climits>
+// kernels.  gate/up: grid (32-row chunks of inter, slots); a warp owns a
+// 4-row group of BOTH matrices of one slot (they share x, staged once per
+// CTA in shared memory) and writes act = silu(g) * u.  As soon as a gate/up
+// CTA knows its expert it also asks L2 to prefetch its share of that
+// expert's down projection, so those bytes stream from HBM while gate/up
+// runs.  down: a CTA owns kDownR 4-row groups of the output and its warp w
+// the slots w, w + W, ...; per slot a warp forms the row dots with act and
+// scales them by rs and the router weight; the per-warp sums are reduced in
+// shared memory in warp order (deterministic).
+//
+// act rows are (inter + 3) / 4 * 4 floats apart, the tail zero-filled, so
+// every float4 of act the down kernel reads is aligned and inside its row.
+//
+// All three kernels are programmatic dependent launches (qmv_internal.cuh):
+// the gate/up CTAs become resident while the select runs, and the down CTAs
+// load their first codes while gate/up runs.
+#include <mutex>
 
 #include "q8_block.cuh"
+#include "tma_util.cuh"
 
 namespace {
 
+// ---------------------------------------------------------------- select
+
 constexpr int kSelThreads = 256;
-constexpr int kSelMaxPerThread = 4;   // n_exp <= 1024
+constexpr int kSelMaxExperts = 1024;
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = a + b;
@@ -32,217 +50,381 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     e = (a - (s - bb)) + (b - bb);
 }
 
-// (value, index) better-than: larger value, or equal value and lower index.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
+// Order-preserving key of a non-NaN float: a > b exactly when key(a) >
+// key(b), with -0 mapped to +0.  Every such key is at least 0x007fffff, so
+// 0 marks "not a candidate".
+__device__ __forceinline__ uint32_t order_key(float v) {
+    uint32_t u = __float_as_uint(v);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kSelThreads) moe_select_kernel(
-    const float* __restrict__ logits, int n, int k, int renorm, const float* __restrict__ sgw,
-    const float* __restrict__ x, int hidden, const float* __restrict__ sg_logit, int32_t* __restrict__ sel,
-    float* __restrict__ wout) {
-    __shared__ float s_a[kSelThreads / 32];
-    __shared__ float s_b[kSelThreads / 32];
-    __shared__ int s_i[kSelThreads / 32];
-    __shared__ float s_gate;
-    __shared__ int s_pick;
-    __shared__ float s_wsel[1024];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    constexpr int nw = kSelThreads / 32;
+// Warp reduction of compensated partial sums (s, c) with TwoSum; the result
+// s + c is the same in every lane.
+__device__ __forceinline__ void warp_sum_comp(float& s, float& c) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float so = __shfl_xor_sync(0xffffffffu, s, off);
+        const float co = __shfl_xor_sync(0xffffffffu, c, off);
+        float t, e;
+        two_sum(s, so, t, e);
+        s = t;
+        c += co + e;
+    }
+}
 
-    // ---- shared-expert gate: compensated dot product (Dot2) ----
-    if (sgw) {
-        float s = 0.f, c = 0.f;
-        for (int i = tid; i < hidden; i += kSelThreads) {
-            const float a = sgw[i], b = x[i];
-            const float p = a * b;
-            const float pe = fmaf(a, b, -p);
-            float t, e;
-            two_sum(s, p, t, e);
-            s = t;
-            c += e + pe;
-        }
-        for (int off = 16; off > 0; off >>= 1) {
-            const float so = __shfl_xor_sync(0xffffffffu, s, off);
-            const float co = __shfl_xor_sync(0xffffffffu, c, off);
-            float t, e;
-            two_sum(s, so, t, e);
-            s = t;
-            c += co + e;
-        }
-        if (lane == 0) { s_a[wid] = s; s_b[wid] = c; }
-        __syncthreads();
-        if (tid == 0) {
-            float ss = s_a[0], cc = s_b[0];
-            for (int w = 1; w < nw; ++w) {
-                float t, e;
-                two_sum(ss, s_a[w], t, e);
-                ss = t;
-                cc += s_b[w] + e;
+// Top-k of logits[0..n), n <= 32 * NPL, by one warp in k rounds of argmax.
+// Lane 0 writes the chosen index of round s to s_sel[s] and its logit to
+// s_val[s].
+template <int NPL>
+__device__ __forceinline__ void topk_warp(const float* logits, int n, int k, int lane, int* s_sel, float* s_val) {
+    float v[NPL];
+    uint32_t key[NPL];
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+        const int idx = lane + 32 * j;
+        v[j] = idx < n ? __ldcg(logits + idx) : 0.f;
+        key[j] = idx < n ? order_key(v[j]) : 0u;
+    }
+    for (int s = 0; s < k; ++s) {
+        uint32_t bk = 0u;
+        int bj = 0;
+        float bv = 0.f;
+#pragma unroll
+        for (int j = 0; j < NPL; ++j)
+            if (key[j] > bk) {   // strict: the lowest j keeps equal keys
+                bk = key[j];
+                bj = j;
+                bv = v[j];
             }
-            s_gate = ss + cc;
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t win =
+            __reduce_min_sync(0xffffffffu, bk == kmax ? (uint32_t)(lane + 32 * bj) : 0xffffffffu);
+        const int wl = (int)(win & 31u);
+        const float val = __shfl_sync(0xffffffffu, bv, wl);
+        if (lane == wl) {
+            const int wj = (int)(win >> 5);
+#pragma unroll
+            for (int j = 0; j < NPL; ++j)
+                if (j == wj) key[j] = 0u;
         }
-        __syncthreads();
-    } else if (sg_logit) {
-        if (tid == 0) s_gate = *sg_logit;
-        __syncthreads();
+        if (lane == 0) {
+            s_sel[s] = (int)win;
+            s_val[s] = val;
+        }
     }
+}
 
-    // ---- logits, max, softmax denominator ----
-    float v[kSelMaxPerThread];
-    bool live[kSelMaxPerThread];
-    float m = -FLT_MAX;
+__device__ __forceinline__ void dot2_step(float a, float b, float& s, float& c) {
+    const float p = a * b;
+    const float pe = fmaf(a, b, -p);
+    float t, e;
+    two_sum(s, p, t, e);
+    s = t;
+    c += e + pe;
+}
+
+// Compensated partial of sum_i sgw[i] * x[i] over i = t, t + nt, ...; every
+// load of a batch of 4 per operand is issued before its arithmetic.
+__device__ __forceinline__ void dot2_part(const float* __restrict__ sgw, const float* x, int hidden, int vec4, int t,
+                                          int nt, float& s, float& c) {
+    s = 0.f;
+    c = 0.f;
+    if (vec4) {
+        const float4* a4 = reinterpret_cast<const float4*>(sgw);
+        const float4* b4 = reinterpret_cast<const float4*>(x);
+        const int n4 = hidden >> 2;
+        for (int i0 = t; i0 < n4; i0 += 4 * nt) {
+            float4 a[4], b[4];
 #pragma unroll
-    for (int j = 0; j < kSelMaxPerThread; ++j) {
-        const int idx = tid + j * kSelThreads;
-        live[j] = idx < n;
-        v[j] = live[j] ? logits[idx] : -FLT_MAX;
-        if (live[j]) m = fmaxf(m, v[j]);
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * nt;
+                a[j] = i < n4 ? __ldg(a4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                b[j] = i < n4 ? __ldcg(b4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                dot2_step(a[j].x, b[j].x, s, c);
+                dot2_step(a[j].y, b[j].y, s, c);
+                dot2_step(a[j].z, b[j].z, s, c);
+                dot2_step(a[j].w, b[j].w, s, c);
+            }
+        }
+    } else {
+        for (int i0 = t; i0 < hidden; i0 += 4 * nt) {
+            float a[4], b[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * nt;
+                a[j] = i < hidden ? __ldg(sgw + i) : 0.f;
+                b[j] = i < hidden ? __ldcg(x + i) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dot2_step(a[j], b[j], s, c);
+        }
     }
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) s_a[wid] = m;
+}
+
+constexpr int kRankMax = 256;   // n_exp up to this: one thread ranks one logit
+
+// Shared-memory state of one router selection.
+struct SelectSmem {
+    uint32_t key[kRankMax];
+    int sel[kSelMaxExperts];
+    float val[kSelMaxExperts];   // logit of the expert chosen in round s
+    float e[kSelMaxExperts];     // exp(val - max)
+    float ps[kSelThreads / 32], pc[kSelThreads / 32];   // gate dot partials
+    float ds[kSelThreads / 32], dc[kSelThreads / 32];   // softmax denominator partials
+};
+
+// The whole router selection, by all kSelThreads threads of a CTA.  On
+// return (in warp 0 only) *norm is the divisor of S.e[0..k) and *gate the
+// shared-expert gate logit (when sgw or sg_logit is given).
+//
+// n <= kRankMax: thread t holds logit t and counts the logits that come
+// before it in the order (value descending, index ascending) -- its rank;
+// rank s < k is the choice of round s of the argmax rounds, since that order
+// is total.  Larger n: warp 0 runs the argmax rounds.  With n <= 128, warps
+// 4..7 form the gate dot while warps 0..3 rank.
+__device__ __forceinline__ void select_block(const float* logits, int n, int k, int renorm,
+                                             const float* __restrict__ sgw, const float* x, int hidden, int vec4,
+                                             const float* sg_logit, SelectSmem& S, float* norm, float* gate) {
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const bool rank_path = n <= kRankMax;
+    const bool dot_side = sgw && n <= 128;
+    float my_v = 0.f;
+    uint32_t my_key = 0u;
+    if (rank_path) {
+        if (tid < n) {
+            my_v = __ldcg(logits + tid);
+            my_key = order_key(my_v);
+        }
+        S.key[tid] = my_key;   // 0 past n: never counted
+    }
+    if (dot_side && tid >= 128) {
+        float s, c;
+        dot2_part(sgw, x, hidden, vec4, tid - 128, kSelThreads - 128, s, c);
+        warp_sum_comp(s, c);
+        if (lane == 0) {
+            S.ps[wid] = s;
+            S.pc[wid] = c;
+        }
+    }
     __syncthreads();
-    float mx = s_a[0];
-    for (int w = 1; w < nw; ++w) mx = fmaxf(mx, s_a[w]);
+    if (rank_path) {
+        if (tid < n) {
+            int rank = 0;
+            const uint4* k4 = reinterpret_cast<const uint4*>(S.key);
+            const int n4 = (n + 3) >> 2;
+            for (int q = 0; q < n4; ++q) {
+                const uint4 kk = k4[q];
+                const int j = 4 * q;
+                rank += (kk.x > my_key) | ((kk.x == my_key) & (j < tid));
+                rank += (kk.y > my_key) | ((kk.y == my_key) & (j + 1 < tid));
+                rank += (kk.z > my_key) | ((kk.z == my_key) & (j + 2 < tid));
+                rank += (kk.w > my_key) | ((kk.w == my_key) & (j + 3 < tid));
+            }
+            if (rank < k) {
+                S.sel[rank] = tid;
+                S.val[rank] = my_v;
+            }
+        }
+    } else if (wid == 0) {
+        if (n <= 512) topk_warp<16>(logits, n, k, lane, S.sel, S.val);
+        else topk_warp<32>(logits, n, k, lane, S.sel, S.val);
+    }
+    if (sgw && !dot_side) {
+        float s, c;
+        dot2_part(sgw, x, hidden, vec4, tid, kSelThreads, s, c);
+        warp_sum_comp(s, c);
+        if (lane == 0) {
+            S.ps[wid] = s;
+            S.pc[wid] = c;
+        }
+    }
     __syncthreads();
-    // softmax denominator: compensated (TwoSum) summation, so its error is
-    // ~1 ulp however many logits there are
-    float es = 0.f, ec = 0.f;
-#pragma unroll
-    for (int j = 0; j < kSelMaxPerThread; ++j)
-        if (live[j]) {
+    const float mx = S.val[0];   // the first choice is the largest logit
+    for (int s = tid; s < k; s += kSelThreads) S.e[s] = expf(S.val[s] - mx);
+    if (!renorm) {
+        // softmax denominator over all n logits, compensated
+        float es = 0.f, ec = 0.f;
+        for (int i = tid; i < n; i += kSelThreads) {
             float t, e;
-            two_sum(es, expf(v[j] - mx), t, e);
+            two_sum(es, expf((rank_path ? my_v : __ldcg(logits + i)) - mx), t, e);
             es = t;
             ec += e;
         }
-    for (int off = 16; off > 0; off >>= 1) {
-        const float so = __shfl_xor_sync(0xffffffffu, es, off);
-        const float co = __shfl_xor_sync(0xffffffffu, ec, off);
-        float t, e;
-        two_sum(es, so, t, e);
-        es = t;
-        ec += co + e;
+        warp_sum_comp(es, ec);
+        if (lane == 0) {
+            S.ds[wid] = es;
+            S.dc[wid] = ec;
+        }
     }
-    if (lane == 0) { s_a[wid] = es; s_b[wid] = ec; }
     __syncthreads();
-    float den_s = s_a[0], den_c = s_b[0];
-    for (int w = 1; w < nw; ++w) {
-        float t, e;
-        two_sum(den_s, s_a[w], t, e);
-        den_s = t;
-        den_c += s_b[w] + e;
-    }
-    const float den = den_s + den_c;
-
-    // ---- k rounds of block argmax over the unchosen logits ----
-    bool chosen[kSelMaxPerThread] = {false, false, false, false};
-    for (int s = 0; s < k; ++s) {
-        float bv = -FLT_MAX;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < kSelMaxPerThread; ++j) {
-            const int idx = tid + j * kSelThreads;
-            if (live[j] && !chosen[j] && (bi == INT_MAX || better(v[j], idx, bv, bi))) {
-                bv = v[j];
-                bi = idx;
-            }
-        }
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (oi != INT_MAX && (bi == INT_MAX || better(ov, oi, bv, bi))) { bv = ov; bi = oi; }
-        }
-        __syncthreads();  // previous round's s_a / s_i reads are done
-        if (lane == 0) { s_a[wid] = bv; s_i[wid] = bi; }
-        __syncthreads();
-        if (tid == 0) {
-            float fv = s_a[0];
-            int fi = s_i[0];
-            for (int w = 1; w < nw; ++w)
-                if (s_i[w] != INT_MAX && (fi == INT_MAX || better(s_a[w], s_i[w], fv, fi))) {
-                    fv = s_a[w];
-                    fi = s_i[w];
-                }
-            s_pick = fi;
-            sel[s] = fi;
-            s_wsel[s] = expf(fv - mx);   // unnormalised; divided below
-        }
-        __syncthreads();
-        const int pick = s_pick;
-#pragma unroll
-        for (int j = 0; j < kSelMaxPerThread; ++j)
-            if (tid + j * kSelThreads == pick) chosen[j] = true;
-    }
-
-    if (tid == 0) {
+    if (wid != 0) return;
+    if (renorm) {
         // renormalised weights are e_s / sum_selected e (the softmax
         // denominator cancels); the selected sum is compensated as well
         float ws = 0.f, wc = 0.f;
-        for (int s = 0; s < k; ++s) {
+        for (int s = lane; s < k; s += 32) {
             float t, e;
-            two_sum(ws, s_wsel[s], t, e);
+            two_sum(ws, S.e[s], t, e);
             ws = t;
             wc += e;
         }
-        const float norm = renorm ? ws + wc : den;
-        for (int s = 0; s < k; ++s) wout[s] = s_wsel[s] / norm;
-        if (sgw || sg_logit) {
-            sel[k] = n;
-            wout[k] = 1.0f / (1.0f + expf(-s_gate));
+        warp_sum_comp(ws, wc);
+        *norm = ws + wc;
+    } else {
+        float ss = S.ds[0], cc = S.dc[0];
+        for (int w = 1; w < kSelThreads / 32; ++w) {
+            float t, e;
+            two_sum(ss, S.ds[w], t, e);
+            ss = t;
+            cc += S.dc[w] + e;
         }
+        *norm = ss + cc;
+    }
+    if (sgw) {
+        const int w0 = dot_side ? 4 : 0;
+        float ss = S.ps[w0], cc = S.pc[w0];
+        for (int w = w0 + 1; w < kSelThreads / 32; ++w) {
+            float t, e;
+            two_sum(ss, S.ps[w], t, e);
+            ss = t;
+            cc += S.pc[w] + e;
+        }
+        *gate = ss + cc;
+    } else if (sg_logit) {
+        *gate = __ldcg(sg_logit);
     }
 }
 
-// ---- expert FFN ----
+__global__ void __launch_bounds__(kSelThreads) moe_select_kernel(
+    const float* logits, int n, int k, int renorm, const float* __restrict__ sgw, const float* x, int hidden,
+    int vec4, const float* sg_logit, int32_t* sel, float* wout) {
+    __shared__ __align__(16) SelectSmem S;
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+    float norm = 1.f, gate = 0.f;
+    select_block(logits, n, k, renorm, sgw, x, hidden, vec4, sg_logit, S, &norm, &gate);
+    if ((threadIdx.x >> 5) != 0) return;
+    const int lane = threadIdx.x & 31;
+    for (int s = lane; s < k; s += 32) {
+        sel[s] = S.sel[s];
+        wout[s] = S.e[s] / norm;
+    }
+    if (lane == 0 && (sgw || sg_logit)) {
+        sel[k] = n;
+        wout[k] = 1.0f / (1.0f + expf(-gate));
+    }
+}
+
+// ---------------------------------------------------------------- expert FFN
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int64_t kXSmemMax = 12288;   // x staged in shared memory up to 48 KB
+constexpr int kDownMaxWarps = 16;
+constexpr int kDownR = 2;              // 4-row groups per down CTA
+constexpr int kDownU = 6;              // 128-column blocks per load batch (768 columns)
 
-// grid.x: row-group chunks of `inter`, grid.y: slot.  act[slot][row].
+// x float4 number `i` (columns 4i..4i+3), zero past `cols`.
+__device__ __forceinline__ float4 x_f4(const float* x, int64_t i, int64_t cols) {
+    const int64_t c = 4 * i;
+    if (c + 4 <= cols) return __ldcg(reinterpret_cast<const float4*>(x) + i);
+    float4 v;
+    v.x = c < cols ? __ldcg(x + c) : 0.f;
+    v.y = c + 1 < cols ? __ldcg(x + c + 1) : 0.f;
+    v.z = c + 2 < cols ? __ldcg(x + c + 2) : 0.f;
+    v.w = c + 3 < cols ? __ldcg(x + c + 3) : 0.f;
+    return v;
+}
+
+// grid.x: 32-row chunks of inter, grid.y: slot.  act[slot][act_stride].
+template <bool kSmemX>
 __global__ void __launch_bounds__(kThreads) moe_gate_up_kernel(
     const int8_t* __restrict__ gq, const float* __restrict__ grs, const int8_t* __restrict__ uq,
     const float* __restrict__ urs, int64_t n_experts, int64_t inter, int64_t rows_pad, int64_t cols_pad,
-    int64_t hidden, const int32_t* __restrict__ sel, const float* __restrict__ x, float* __restrict__ act,
-    int* __restrict__ status) {
+    int64_t hidden, const int8_t* __restrict__ dq, const float* __restrict__ drs, int64_t d_rows_pad,
+    int64_t d_cols_pad, const int32_t* sel, const float* x, float* act, int64_t act_stride, int* status) {
+    extern __shared__ float4 xsm[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int slot = blockIdx.y;
     const int64_t rg = (int64_t)blockIdx.x * kWarps + warp;
-    if (rg * 4 >= inter) return;
-    const int e = sel[slot];
-    if (e < 0 || e >= n_experts) {
+    const bool live = rg * 4 < inter;
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+
+    const int e = __ldcg(sel + slot);
+    const bool ok = e >= 0 && e < n_experts;
+    if (ok && threadIdx.x == 0) {
+        // this CTA's share of the expert's down projection, into L2
+        const int64_t total = d_rows_pad * d_cols_pad;   // a multiple of 16
+        const int64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) & ~(int64_t)15;
+        const int64_t b0 = (int64_t)blockIdx.x * share;
+        const int64_t b1 = b0 + share < total ? b0 + share : total;
+        const int8_t* base = dq + (int64_t)e * total;
+        for (int64_t o = b0; o < b1; o += 65536)
+            qmv::prefetch_l2(base + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+        if (blockIdx.x == 0) qmv::prefetch_l2(drs + (int64_t)e * d_rows_pad, (uint32_t)(d_rows_pad * 4));
+    }
+    if (ok && threadIdx.x == 32) {
+        // this CTA's own gate and up rows: all requested at once, so HBM sees
+        // the whole working set instead of one load batch per warp
+        const int64_t r0 = (int64_t)blockIdx.x * kWarps * 4;
+        const int64_t r1 = r0 + kWarps * 4 < rows_pad ? r0 + kWarps * 4 : rows_pad;
+        if (r1 > r0) {
+            const int64_t off = (int64_t)e * rows_pad * cols_pad + r0 * cols_pad;
+            const int64_t bytes = (r1 - r0) * cols_pad;
+            for (int64_t o = 0; o < bytes; o += 65536) {
+                const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+                qmv::prefetch_l2(gq + off + o, n);
+                qmv::prefetch_l2(uq + off + o, n);
+            }
+        }
+    }
+    if constexpr (kSmemX) {
+        for (int64_t i = threadIdx.x; i < cols_pad / 4; i += kThreads) xsm[i] = x_f4(x, i, hidden);
+        __syncthreads();
+    }
+    if (!live) return;
+    if (!ok) {
         if (lane == 0) atomicCAS(status, 0, qmv::kDevBadExpert);
-        if (lane < 4 && rg * 4 + lane < inter) act[slot * inter + rg * 4 + lane] = 0.f;
+        if (lane < 4) act[(int64_t)slot * act_stride + rg * 4 + lane] = 0.f;
         return;
     }
+
     const int64_t nblk = cols_pad / 128;
-    const int8_t* gbase = gq + (int64_t)e * rows_pad * cols_pad;
-    const int8_t* ubase = uq + (int64_t)e * rows_pad * cols_pad;
+    const int8_t* pg = gq + (int64_t)e * rows_pad * cols_pad + rg * 4 * cols_pad + lane * 16;
+    const int8_t* pu = uq + (int64_t)e * rows_pad * cols_pad + rg * 4 * cols_pad + lane * 16;
+    auto xblk = [&](int64_t b) -> float4 {
+        if constexpr (kSmemX) return xsm[b * 32 + lane];
+        else return x_f4(x, b * 32 + lane, hidden);
+    };
     float2 ag[4], au[4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) { ag[r] = make_float2(0.f, 0.f); au[r] = make_float2(0.f, 0.f); }
-    const int8_t* pg = gbase + rg * 4 * cols_pad + lane * 16;
-    const int8_t* pu = ubase + rg * 4 * cols_pad + lane * 16;
-    int64_t b = 0;
+    for (int r = 0; r < 4; ++r) {
+        ag[r] = make_float2(0.f, 0.f);
+        au[r] = make_float2(0.f, 0.f);
+    }
     constexpr int U = 4;
+    int64_t b = 0;
     for (; b + U <= nblk; b += U) {
         uint4 wg[U], wu[U];
-        float4 xv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             wg[u] = qmv::ld_stream_u4(pg + (b + u) * 512);
             wu[u] = qmv::ld_stream_u4(pu + (b + u) * 512);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) xv[u] = qmv::act_for_block(x, b + u, lane, hidden);
-#pragma unroll
         for (int u = 0; u < U; ++u) {
-            qmv::q8_chunk_fma(wg[u], xv[u], ag);
-            qmv::q8_chunk_fma(wu[u], xv[u], au);
+            const float4 xv = xblk(b + u);
+            qmv::q8_chunk_fma(wg[u], xv, ag);
+            qmv::q8_chunk_fma(wu[u], xv, au);
         }
     }
     for (; b < nblk; ++b) {
-        const float4 xv = qmv::act_for_block(x, b, lane, hidden);
+        const float4 xv = xblk(b);
         qmv::q8_chunk_fma(qmv::ld_stream_u4(pg + b * 512), xv, ag);
         qmv::q8_chunk_fma(qmv::ld_stream_u4(pu + b * 512), xv, au);
     }
@@ -253,56 +435,469 @@ __global__ void __launch_bounds__(kThreads) moe_gate_up_kernel(
         u[r] = qmv::warp_sum(au[r].x + au[r].y);
     }
     if (lane < 4) {
-        const int64_t row = rg * 4 + lane;
+        const int64_t row = rg * 4 + lane;   // < act_stride
+        float a = 0.f;
         if (row < inter) {
             const float gs = (lane == 0 ? g[0] : lane == 1 ? g[1] : lane == 2 ? g[2] : g[3]) *
                              grs[(int64_t)e * rows_pad + row];
             const float us = (lane == 0 ? u[0] : lane == 1 ? u[1] : lane == 2 ? u[2] : u[3]) *
                              urs[(int64_t)e * rows_pad + row];
-            act[slot * inter + row] = gs / (1.0f + expf(-gs)) * us;
+            a = gs / (1.0f + expf(-gs)) * us;
+        }
+        act[(int64_t)slot * act_stride + row] = a;
+    }
+}
+
+// Codes of row groups rg0 .. rg0 + kDownR - 1, blocks b0 .. b0 + kDownU - 1,
+// of expert e (zero where out of range or !ok).
+__device__ __forceinline__ void down_codes(uint4 (&w)[kDownR][kDownU], const int8_t* __restrict__ dq, int e,
+                                           bool ok, int64_t rows_pad, int64_t cols_pad, int64_t rg0, int64_t n_rg,
+                                           int64_t b0, int64_t nblk, int lane) {
+    const int8_t* base = dq + (int64_t)(ok ? e : 0) * rows_pad * cols_pad + lane * 16;
+#pragma unroll
+    for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+        for (int u = 0; u < kDownU; ++u) {
+            const int64_t rg = rg0 + r, b = b0 + u;
+            w[r][u] = (ok && rg < n_rg && b < nblk) ? qmv::ld_stream_u4(base + rg * 4 * cols_pad + b * 512)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        }
+}
+
+// Per-row factor w[s] * rs[e][row] of this CTA's rows (0 where out of range or !ok).
+__device__ __forceinline__ void down_scales(float (&f)[kDownR][4], const float* __restrict__ drs,
+                                            const float* wsel, int s, int e, bool ok, int64_t rows_pad,
+                                            int64_t hidden, int64_t rg0) {
+    const float ws = ok ? __ldcg(wsel + s) : 0.f;
+#pragma unroll
+    for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t row = (rg0 + r) * 4 + i;
+            f[r][i] = ok && row < hidden ? ws * __ldg(drs + (int64_t)e * rows_pad + row) : 0.f;
+        }
+}
+
+// CTA: row groups blockIdx.x * kDownR + r; warp w: slots w, w + W, ...
+// 112 registers: two CTAs of 9 warps (top-8 + shared) fit on an SM.
+__global__ void __maxnreg__(112) moe_down_kernel(
+    const int8_t* __restrict__ dq, const float* __restrict__ drs, int64_t n_experts, int64_t hidden,
+    int64_t rows_pad, int64_t cols_pad, const int32_t* sel, const float* wsel, int slots, const float* act,
+    int64_t act_stride, float* out) {
+    __shared__ float part[kDownMaxWarps][kDownR * 4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int64_t rg0 = (int64_t)blockIdx.x * kDownR;
+    const int64_t n_rg = (hidden + 3) / 4;
+    const int64_t nblk = cols_pad / 128;
+
+    // Before the dependency wait: the first slot's expert, router weight, row
+    // scales and first codes.  sel and w were final before the gate/up kernel
+    // of this call passed its own wait, and this grid launched only after that.
+    int s = warp;
+    int e = s < slots ? __ldcg(sel + s) : -1;
+    bool ok = e >= 0 && e < n_experts;
+    uint4 w[kDownR][kDownU];
+    float f[kDownR][4];
+    down_codes(w, dq, e, ok, rows_pad, cols_pad, rg0, n_rg, 0, nblk, lane);
+    down_scales(f, drs, wsel, s, e, ok, rows_pad, hidden, rg0);
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+
+    float tot[kDownR][4];
+#pragma unroll
+    for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tot[r][i] = 0.f;
+    for (; s < slots; s += nw) {
+        if (s != warp) {
+            e = __ldcg(sel + s);
+            ok = e >= 0 && e < n_experts;
+            down_codes(w, dq, e, ok, rows_pad, cols_pad, rg0, n_rg, 0, nblk, lane);
+            down_scales(f, drs, wsel, s, e, ok, rows_pad, hidden, rg0);
+        }
+        if (!ok) continue;   // reported by the gate/up kernel
+        float2 acc[kDownR][4];
+#pragma unroll
+        for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[r][i] = make_float2(0.f, 0.f);
+        const float* a = act + (int64_t)s * act_stride;
+        for (int64_t b0 = 0; b0 < nblk; b0 += kDownU) {
+            if (b0 > 0) down_codes(w, dq, e, ok, rows_pad, cols_pad, rg0, n_rg, b0, nblk, lane);
+            float4 av[kDownU];
+#pragma unroll
+            for (int u = 0; u < kDownU; ++u) {
+                const int64_t c = (b0 + u) * 128 + lane * 4;
+                av[u] = c < act_stride ? __ldcg(reinterpret_cast<const float4*>(a + c))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+                for (int u = 0; u < kDownU; ++u) qmv::q8_chunk_fma(w[r][u], av[u], acc[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) tot[r][i] = fmaf(f[r][i], qmv::warp_sum(acc[r][i].x + acc[r][i].y), tot[r][i]);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < kDownR; ++r)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) part[warp][r * 4 + i] = tot[r][i];
+    }
+    __syncthreads();
+    if (threadIdx.x < kDownR * 4) {
+        float sum = 0.f;
+        for (int ww = 0; ww < nw; ++ww) sum += part[ww][threadIdx.x];
+        const int64_t row = rg0 * 4 + threadIdx.x;
+        if (row < hidden) out[row] = sum;
+    }
+}
+
+// ---- staged FFN kernels: codes copied into shared memory in bulk ----
+
+constexpr int64_t kFfnSmem = 96 * 1024;   // codes staged per CTA
+constexpr int kGuMaxRG = 8;               // row groups per gate/up CTA
+constexpr int kDnMaxUnits = 64;           // (slot, row group) units per down CTA
+
+// dst[i] = load(i) for i in [0, n), by all threads of the CTA; each thread
+// issues the loads of a batch of kStageBatch before any store, so staging
+// costs one memory round trip per batch instead of one per element.
+constexpr int kStageBatch = 8;
+template <class Load>
+__device__ __forceinline__ void stage_f4(float4* dst, int n, Load load) {
+    for (int i0 = threadIdx.x; i0 < n; i0 += kStageBatch * kThreads) {
+        float4 v[kStageBatch];
+#pragma unroll
+        for (int j = 0; j < kStageBatch; ++j) {
+            const int i = i0 + j * kThreads;
+            v[j] = i < n ? load(i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kStageBatch; ++j) {
+            const int i = i0 + j * kThreads;
+            if (i < n) dst[i] = v[j];
         }
     }
 }
 
-// Warp w: row group blockIdx.x * (kWarps/S) + w / S, slots s = w % S, w % S + S, ...
-__global__ void __launch_bounds__(kThreads) moe_down_kernel(
-    const int8_t* __restrict__ dq, const float* __restrict__ drs, int64_t n_experts, int64_t hidden,
-    int64_t rows_pad, int64_t cols_pad, int64_t inter, const int32_t* __restrict__ sel,
-    const float* __restrict__ wsel, int slots, const float* __restrict__ act, float* __restrict__ out, int S) {
-    __shared__ float part[kWarps * 4];
+// Flattened (unit, 128-column block) range of warp `warp` out of kWarps.
+__device__ __forceinline__ void warp_range(int total, int warp, int& a, int& b) {
+    a = warp * total / kWarps;
+    b = (warp + 1) * total / kWarps;
+}
+
+// gate/up: grid (ceil(n_rg / R), slots).  CTA: row groups [c R, c R + R) of
+// both matrices of the slot's expert, in shared memory as [gate rows][up rows].
+__global__ void __launch_bounds__(kThreads) moe_gate_up_smem_kernel(
+    const int8_t* __restrict__ gq, const float* __restrict__ grs, const int8_t* __restrict__ uq,
+    const float* __restrict__ urs, int64_t n_experts, int64_t inter, int64_t rows_pad, int64_t cols_pad,
+    int64_t hidden, int R, const int8_t* __restrict__ dq, const float* __restrict__ drs, int64_t d_rows_pad,
+    int64_t d_cols_pad, const int32_t* sel, const float* x, float* act, int64_t act_stride, int* status) {
+    extern __shared__ __align__(128) uint8_t smc[];   // [gate rows][up rows][x]
+    __shared__ __align__(8) uint64_t bar[kGuMaxRG];
+    __shared__ float part[kGuMaxRG][kWarps][8];   // per warp: gate[4], up[4]
+    __shared__ int abort_flag;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gpc = kWarps / S;
-    const int ks = warp % S, rgl = warp / S;
-    const int64_t rg = (int64_t)blockIdx.x * gpc + rgl;
-    const int64_t nblk = cols_pad / 128;
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
-    if (rg * 4 < hidden) {
-        for (int s = ks; s < slots; s += S) {
-            const int e = sel[s];
-            if (e < 0 || e >= n_experts) continue;  // reported by the gate/up kernel
-            float v[4];
-            qmv::q8_rowgroup_dot<2>(dq + (int64_t)e * rows_pad * cols_pad, cols_pad, rg, 0, nblk,
-                                    act + (int64_t)s * inter, inter, lane, v);
-            const float ws = wsel[s];
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int64_t row = rg * 4 + r;
-                const float rsv = row < hidden ? drs[(int64_t)e * rows_pad + row] : 0.f;
-                tot[r] = fmaf(ws * rsv, qmv::warp_sum(v[r]), tot[r]);
+    const int slot = blockIdx.y;
+    const int64_t n_rg = (inter + 3) / 4;
+    const int64_t g0 = (int64_t)blockIdx.x * R;
+    const int Rc = (int)(n_rg - g0 < R ? n_rg - g0 : R);
+    const int64_t rgb = 4 * cols_pad;
+    const int nblk = (int)(cols_pad / 128);
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int r = 0; r < Rc; ++r) qmv::mbar_init(&bar[r], 1);
+        qmv::mbar_fence_init();
+    }
+    for (int i = threadIdx.x; i < Rc * kWarps * 8; i += kThreads) (&part[0][0][0])[i] = 0.f;
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+    __syncthreads();
+
+    const int e = __ldcg(sel + slot);
+    if (e < 0 || e >= n_experts) {
+        if (threadIdx.x == 0) atomicCAS(status, 0, qmv::kDevBadExpert);
+        for (int t = threadIdx.x; t < Rc * 4; t += kThreads) act[(int64_t)slot * act_stride + g0 * 4 + t] = 0.f;
+        return;   // no copy was issued
+    }
+    if (threadIdx.x == 0) {
+        const int64_t src = (int64_t)e * rows_pad * cols_pad + g0 * rgb;
+        for (int r = 0; r < Rc; ++r) {
+            qmv::mbar_arrive_tx(&bar[r], (uint32_t)(2 * rgb));
+            for (int64_t o = 0; o < rgb; o += 32768) {
+                const uint32_t n = (uint32_t)(rgb - o < 32768 ? rgb - o : 32768);
+                qmv::bulk_g2s(smc + r * rgb + o, gq + src + r * rgb + o, n, &bar[r]);
+                qmv::bulk_g2s(smc + (Rc + r) * rgb + o, uq + src + r * rgb + o, n, &bar[r]);
             }
         }
+    } else if (threadIdx.x == 32) {
+        // this CTA's share of the expert's down projection, into L2, so the
+        // down kernel finds it there
+        const int64_t total = d_rows_pad * d_cols_pad;   // a multiple of 16
+        const int64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) & ~(int64_t)15;
+        const int64_t b0 = (int64_t)blockIdx.x * share;
+        const int64_t b1 = b0 + share < total ? b0 + share : total;
+        const int8_t* base = dq + (int64_t)e * total;
+        for (int64_t o = b0; o < b1; o += 65536)
+            qmv::prefetch_l2(base + o, (uint32_t)(b1 - o < 65536 ? b1 - o : 65536));
+        if (blockIdx.x == 0) qmv::prefetch_l2(drs + (int64_t)e * d_rows_pad, (uint32_t)(d_rows_pad * 4));
     }
-    if (lane == 0) {
+
+    // x, zero-padded to cols_pad, loaded once per CTA while the codes stream in
+    float4* xs4 = reinterpret_cast<float4*>(smc + 2 * (int64_t)R * rgb);
+    stage_f4(xs4, nblk * 32, [&](int i) { return qmv::act_for_block(x, i >> 5, i & 31, hidden); });
+    __syncthreads();
+
+    int a, b;
+    warp_range(Rc * nblk, warp, a, b);
+    for (int i = a; i < b;) {
+        const int r = i / nblk;
+        const int bs = i - r * nblk;
+        const int be = b - r * nblk < nblk ? b - r * nblk : nblk;
+        if (!qmv::mbar_wait(&bar[r], 0, &abort_flag, status)) break;
+        const uint8_t* gb = smc + r * rgb + lane * 16;
+        const uint8_t* ub = smc + (Rc + r) * rgb + lane * 16;
+        float2 ag[4], au[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) part[(ks * gpc + rgl) * 4 + r] = tot[r];
+        for (int k = 0; k < 4; ++k) {
+            ag[k] = make_float2(0.f, 0.f);
+            au[k] = make_float2(0.f, 0.f);
+        }
+#pragma unroll 4
+        for (int blk = bs; blk < be; ++blk) {
+            const float4 xv = xs4[blk * 32 + lane];
+            qmv::q8_chunk_fma(*reinterpret_cast<const uint4*>(gb + blk * 512), xv, ag);
+            qmv::q8_chunk_fma(*reinterpret_cast<const uint4*>(ub + blk * 512), xv, au);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float gv = qmv::warp_sum(ag[k].x + ag[k].y);
+            const float uv = qmv::warp_sum(au[k].x + au[k].y);
+            if (lane == 0) {
+                part[r][warp][k] = gv;
+                part[r][warp][4 + k] = uv;
+            }
+        }
+        i = r * nblk + be;
     }
     __syncthreads();
-    if (threadIdx.x < gpc * 4) {
-        float s = 0.f;
-        for (int k = 0; k < S; ++k) s += part[k * gpc * 4 + threadIdx.x];
-        const int64_t row = (int64_t)blockIdx.x * gpc * 4 + threadIdx.x;
-        if (row < hidden) out[row] = s;
+    if (abort_flag) {
+        // a wait gave up: let every copy land before shared memory is released
+        if (threadIdx.x == 0)
+            for (int r = 0; r < Rc; ++r) qmv::mbar_drain(&bar[r], 0);
+        return;
     }
+    for (int t = threadIdx.x; t < Rc * 4; t += kThreads) {
+        const int r = t >> 2, k = t & 3;
+        float g = 0.f, u = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            g += part[r][w][k];
+            u += part[r][w][4 + k];
+        }
+        const int64_t row = (g0 + r) * 4 + k;   // < act_stride
+        float v = 0.f;
+        if (row < inter) {
+            const float gs = g * grs[(int64_t)e * rows_pad + row];
+            const float us = u * urs[(int64_t)e * rows_pad + row];
+            v = gs / (1.0f + expf(-gs)) * us;
+        }
+        act[(int64_t)slot * act_stride + row] = v;
+    }
+}
+
+// down: CTA c owns output row groups [c R, c R + R) for every slot; shared
+// memory holds [slot][R row groups] of down codes, then act of every slot.  Everything that depends
+// only on sel and w (codes, row scales, router weights) is fetched before the
+// dependency wait; after it, only act is read.
+__global__ void __launch_bounds__(kThreads) moe_down_smem_kernel(
+    const int8_t* __restrict__ dq, const float* __restrict__ drs, int64_t n_experts, int64_t hidden,
+    int64_t rows_pad, int64_t cols_pad, int R, const int32_t* sel, const float* wsel, int slots, const float* act,
+    int64_t act_stride, float* out, int* status) {
+    extern __shared__ __align__(128) uint8_t smc[];
+    __shared__ __align__(8) uint64_t bar[64];
+    __shared__ float part[kDnMaxUnits][kWarps][4];
+    __shared__ float s_f[kDnMaxUnits * 4];   // w[s] * rs[e_s][row], per (unit, row of its group)
+    __shared__ int s_e[64];
+    __shared__ int abort_flag;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n_rg = (hidden + 3) / 4;
+    const int64_t g0 = (int64_t)blockIdx.x * R;
+    const int Rc = (int)(n_rg - g0 < R ? n_rg - g0 : R);
+    const int64_t rgb = 4 * cols_pad;
+    const int nblk = (int)(cols_pad / 128);
+    const int U = slots * Rc;
+
+    // Before the dependency wait.  sel and w were final before the gate/up
+    // kernel of this call passed its own wait, and this grid launched only
+    // after that.
+    if (threadIdx.x < slots) {
+        const int e = __ldcg(sel + threadIdx.x);
+        s_e[threadIdx.x] = e >= 0 && e < n_experts ? e : -1;
+    }
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < slots; ++s) qmv::mbar_init(&bar[s], 1);
+        qmv::mbar_fence_init();
+    }
+    for (int i = threadIdx.x; i < U * kWarps * 4; i += kThreads) (&part[0][0][0])[i] = 0.f;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < slots; ++s) {
+            const int e = s_e[s];
+            if (e < 0) {   // reported by the gate/up kernel; nothing to fetch
+                qmv::mbar_arrive(&bar[s]);
+                continue;
+            }
+            const int64_t bytes = Rc * rgb;
+            qmv::mbar_arrive_tx(&bar[s], (uint32_t)bytes);
+            const int8_t* src = dq + (int64_t)e * rows_pad * cols_pad + g0 * rgb;
+            for (int64_t o = 0; o < bytes; o += 32768)
+                qmv::bulk_g2s(smc + (int64_t)s * Rc * rgb + o, src + o,
+                              (uint32_t)(bytes - o < 32768 ? bytes - o : 32768), &bar[s]);
+        }
+    }
+    for (int t = threadIdx.x; t < U * 4; t += kThreads) {
+        const int s = t / (Rc * 4), j = t - s * Rc * 4;
+        const int e = s_e[s];
+        const int64_t row = g0 * 4 + j;
+        s_f[t] = e >= 0 && row < hidden ? __ldcg(wsel + s) * drs[(int64_t)e * rows_pad + row] : 0.f;
+    }
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+    // act of every slot, zero-padded to cols_pad, loaded once per CTA
+    float4* as4 = reinterpret_cast<float4*>(smc + (int64_t)U * rgb);
+    stage_f4(as4, slots * nblk * 32, [&](int i) {
+        const int s = i / (nblk * 32);
+        const int64_t c = (int64_t)(i - s * nblk * 32) * 4;
+        return c < act_stride ? __ldcg(reinterpret_cast<const float4*>(act + (int64_t)s * act_stride + c))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    });
+    __syncthreads();
+
+    int a, b;
+    warp_range(U * nblk, warp, a, b);
+    for (int i = a; i < b;) {
+        const int u = i / nblk;
+        const int bs = i - u * nblk;
+        const int be = b - u * nblk < nblk ? b - u * nblk : nblk;
+        const int s = u / Rc;
+        i = u * nblk + be;
+        if (!qmv::mbar_wait(&bar[s], 0, &abort_flag, status)) break;
+        if (s_e[s] < 0) continue;
+        const uint8_t* base = smc + (int64_t)u * rgb + lane * 16;
+        const float4* arow = as4 + s * nblk * 32 + lane;
+        float2 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+#pragma unroll 4
+        for (int blk = bs; blk < be; ++blk)
+            qmv::q8_chunk_fma(*reinterpret_cast<const uint4*>(base + blk * 512), arow[blk * 32], acc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float v = qmv::warp_sum(acc[k].x + acc[k].y);
+            if (lane == 0) part[u][warp][k] = v;
+        }
+    }
+    __syncthreads();
+    if (abort_flag) {
+        if (threadIdx.x == 0)
+            for (int s = 0; s < slots; ++s) qmv::mbar_drain(&bar[s], 0);
+        return;
+    }
+    for (int t = threadIdx.x; t < Rc * 4; t += kThreads) {
+        const int r = t >> 2, k = t & 3;
+        float sum = 0.f;
+        for (int s = 0; s < slots; ++s) {
+            const int u = s * Rc + r;
+            float d = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) d += part[u][w][k];
+            sum = fmaf(s_f[u * 4 + k], d, sum);
+        }
+        const int64_t row = (g0 + r) * 4 + k;
+        if (row < hidden) out[row] = sum;
+    }
+}
+
+int64_t act_stride_of(int64_t inter) { return (inter + 3) / 4 * 4; }
+
+qmv_status check_ffn_args(const char* fn, const qmv_weights* gate, const qmv_weights* up, const qmv_weights* down,
+                          const int32_t* sel, const float* w, int slots, const float* x, const float* out) {
+    QMV_REQUIRE(gate && up && down && sel && w && x && out, QMV_ERR_INVALID_ARG, "%s: null argument", fn);
+    QMV_REQUIRE(gate->format == QMV_FMT_Q8ROW && up->format == QMV_FMT_Q8ROW && down->format == QMV_FMT_Q8ROW,
+                QMV_ERR_UNSUPPORTED, "%s: handles must be q8_row", fn);
+    QMV_REQUIRE(slots >= 1 && slots <= 64, QMV_ERR_INVALID_ARG, "%s: need 1 <= slots <= 64", fn);
+    const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
+    QMV_REQUIRE(up->experts == E && up->rows == inter && up->cols == hidden && down->experts == E &&
+                    down->rows == hidden && down->cols == inter,
+                QMV_ERR_INVALID_ARG,
+                "%s: gate/up [E][inter][hidden] and down [E][hidden][inter] shapes disagree", fn);
+    QMV_REQUIRE(qmv::aligned16(x) && qmv::aligned16(out), QMV_ERR_INVALID_ARG,
+                "%s: x and out must be 16-byte aligned", fn);
+    return QMV_OK;
+}
+
+// The two FFN launches; act: [slots][act_stride_of(inter)] floats, 16-byte aligned.
+qmv_status launch_ffn(const qmv_weights* gate, const qmv_weights* up, const qmv_weights* down,
+                      const int32_t* sel, const float* w, int slots, const float* x, float* out, float* act,
+                      int* status, cudaStream_t cs) {
+    const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
+    const int64_t astride = act_stride_of(inter);
+    const int64_t sms = qmv::sm_count();
+    static int configured[64] = {0};
+    const int dev = qmv::current_device();
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaFuncSetAttribute(moe_gate_up_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFfnSmem);
+        cudaFuncSetAttribute(moe_down_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFfnSmem);
+        configured[dev] = 1;
+    }
+    qmv_status st;
+    // gate/up: about three staged CTAs per SM
+    const int64_t gu_rgb = 4 * gate->cols_pad;
+    const int64_t n_rg_i = (inter + 3) / 4;
+    // codes of gu_r row groups of both matrices, plus x (cols_pad floats = one row group's bytes)
+    int64_t gu_r = (kFfnSmem / gu_rgb - 1) / 2 < kGuMaxRG ? (kFfnSmem / gu_rgb - 1) / 2 : kGuMaxRG;
+    if (gu_r >= 1) {
+        const int64_t want = (slots * n_rg_i + 3 * sms - 1) / (3 * sms);
+        if (gu_r > want) gu_r = want < 1 ? 1 : want;
+        const dim3 g1((unsigned)((n_rg_i + gu_r - 1) / gu_r), (unsigned)slots);
+        st = qmv::launch_pdl(moe_gate_up_smem_kernel, g1, dim3(kThreads), (size_t)((2 * gu_r + 1) * gu_rgb), cs, gate->q,
+                             gate->rs, up->q, up->rs, E, inter, gate->rows_pad, gate->cols_pad, hidden, (int)gu_r,
+                             down->q, down->rs, down->rows_pad, down->cols_pad, sel, x, act, astride, status);
+    } else {
+        const dim3 g1((unsigned)((n_rg_i + kWarps - 1) / kWarps), (unsigned)slots);
+        if (gate->cols_pad <= kXSmemMax) {
+            st = qmv::launch_pdl(moe_gate_up_kernel<true>, g1, dim3(kThreads), (size_t)gate->cols_pad * 4, cs,
+                                 gate->q, gate->rs, up->q, up->rs, E, inter, gate->rows_pad, gate->cols_pad, hidden,
+                                 down->q, down->rs, down->rows_pad, down->cols_pad, sel, x, act, astride, status);
+        } else {
+            st = qmv::launch_pdl(moe_gate_up_kernel<false>, g1, dim3(kThreads), 0, cs, gate->q, gate->rs, up->q,
+                                 up->rs, E, inter, gate->rows_pad, gate->cols_pad, hidden, down->q, down->rs,
+                                 down->rows_pad, down->cols_pad, sel, x, act, astride, status);
+        }
+    }
+    if (st != QMV_OK) return st;
+    // down: all slots of R output row groups per CTA, about two CTAs per SM
+    const int64_t n_rg = (hidden + 3) / 4;
+    const int64_t dn_rgb = 4 * down->cols_pad;
+    // codes of dn_r row groups per slot, plus act (slots x cols_pad floats = one row group's bytes per slot)
+    int64_t dn_r = kFfnSmem / (slots * dn_rgb) - 1;
+    if (dn_r > kDnMaxUnits / slots) dn_r = kDnMaxUnits / slots;
+    if (dn_r >= 1) {
+        const int64_t want = (n_rg + 2 * sms - 1) / (2 * sms);
+        if (dn_r > want) dn_r = want < 1 ? 1 : want;
+        return qmv::launch_pdl(moe_down_smem_kernel, dim3((unsigned)((n_rg + dn_r - 1) / dn_r)), dim3(kThreads),
+                               (size_t)(slots * (dn_r + 1) * dn_rgb), cs, down->q, down->rs, E, hidden, down->rows_pad,
+                               down->cols_pad, (int)dn_r, sel, w, slots, act, astride, out, status);
+    }
+    const int nw = slots < kDownMaxWarps ? slots : kDownMaxWarps;
+    return qmv::launch_pdl(moe_down_kernel, dim3((unsigned)((n_rg + kDownR - 1) / kDownR)), dim3(nw * 32), 0, cs,
+                           down->q, down->rs, E, hidden, down->rows_pad, down->cols_pad, sel, w, slots, act,
+                           astride, out);
 }
 
 }  // namespace
@@ -311,50 +906,33 @@ extern "C" qmv_status moe_select_topk(const float* logits, int n_exp, int top_k,
                                       const float* sg_w, const float* x, int hidden, const float* sg_logit,
                                       int32_t* sel, float* w, qmv_stream st) {
     QMV_REQUIRE(logits && sel && w, QMV_ERR_INVALID_ARG, "moe_select_topk: null argument");
-    QMV_REQUIRE(n_exp >= 1 && n_exp <= kSelThreads * kSelMaxPerThread, QMV_ERR_INVALID_ARG,
-                "moe_select_topk: need 1 <= n_exp <= %d (got %d)", kSelThreads * kSelMaxPerThread, n_exp);
+    QMV_REQUIRE(n_exp >= 1 && n_exp <= kSelMaxExperts, QMV_ERR_INVALID_ARG,
+                "moe_select_topk: need 1 <= n_exp <= %d (got %d)", kSelMaxExperts, n_exp);
     QMV_REQUIRE(top_k >= 1 && top_k <= n_exp, QMV_ERR_INVALID_ARG,
                 "moe_select_topk: need 1 <= top_k <= n_exp (got %d)", top_k);
     QMV_REQUIRE(!sg_w || (x && hidden >= 1), QMV_ERR_INVALID_ARG,
                 "moe_select_topk: sg_w needs x and hidden >= 1");
-    moe_select_kernel<<<1, kSelThreads, 0, (cudaStream_t)st>>>(logits, n_exp, top_k, renorm, sg_w, x, hidden,
-                                                              sg_w ? nullptr : sg_logit, sel, w);
-    return qmv::check_launch("moe_select_kernel");
+    const int vec4 = sg_w && hidden % 4 == 0 && qmv::aligned16(sg_w) && qmv::aligned16(x);
+    return qmv::launch_pdl(moe_select_kernel, dim3(1), dim3(kSelThreads), 0, (cudaStream_t)st, logits, n_exp,
+                           top_k, renorm, sg_w, x, sg_w ? hidden : 0, vec4, sg_w ? nullptr : sg_logit, sel, w);
 }
 
 extern "C" qmv_status moe_ffn_q8row(const qmv_weights* gate, const qmv_weights* up, const qmv_weights* down,
                                     const int32_t* sel, const float* w, int slots, const float* x, float* out,
                                     qmv_stream st) {
-    QMV_REQUIRE(gate && up && down && sel && w && x && out, QMV_ERR_INVALID_ARG, "moe_ffn_q8row: null argument");
-    QMV_REQUIRE(gate->format == QMV_FMT_Q8ROW && up->format == QMV_FMT_Q8ROW && down->format == QMV_FMT_Q8ROW,
-                QMV_ERR_UNSUPPORTED, "moe_ffn_q8row: handles must be q8_row");
-    QMV_REQUIRE(slots >= 1 && slots <= 64, QMV_ERR_INVALID_ARG, "moe_ffn_q8row: need 1 <= slots <= 64");
-    const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
-    QMV_REQUIRE(up->experts == E && up->rows == inter && up->cols == hidden && down->experts == E &&
-                    down->rows == hidden && down->cols == inter,
-                QMV_ERR_INVALID_ARG, "moe_ffn_q8row: gate/up [E][inter][hidden] and down [E][hidden][inter] "
-                                     "shapes disagree");
-    QMV_REQUIRE(qmv::aligned16(x) && qmv::aligned16(out), QMV_ERR_INVALID_ARG,
-                "moe_ffn_q8row: x and out must be 16-byte aligned");
+    const qmv_status a = check_ffn_args("moe_ffn_q8row", gate, up, down, sel, w, slots, x, out);
+    if (a != QMV_OK) return a;
     int* status = qmv::device_status();
     QMV_REQUIRE(status, QMV_ERR_CUDA, "moe_ffn_q8row: no CUDA device");
     cudaStream_t cs = (cudaStream_t)st;
     float* act = nullptr;
-    const size_t act_bytes = (size_t)slots * (size_t)inter * sizeof(float);
+    const size_t act_bytes = (size_t)slots * (size_t)act_stride_of(gate->rows) * sizeof(float);
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&act), act_bytes, cs);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return qmv::fail(QMV_ERR_ALLOC, "moe_ffn_q8row: scratch allocation failed: %s", cudaGetErrorString(e));
     }
-    const dim3 g1((unsigned)(((inter + 3) / 4 + kWarps - 1) / kWarps), (unsigned)slots);
-    moe_gate_up_kernel<<<g1, kThreads, 0, cs>>>(gate->q, gate->rs, up->q, up->rs, E, inter, gate->rows_pad,
-                                                gate->cols_pad, hidden, sel, x, act, status);
-    const int S = slots >= 4 ? 4 : slots >= 2 ? 2 : 1;
-    const int gpc = kWarps / S;
-    const int64_t n_rg = (hidden + 3) / 4;
-    moe_down_kernel<<<(unsigned)((n_rg + gpc - 1) / gpc), kThreads, 0, cs>>>(
-        down->q, down->rs, E, hidden, down->rows_pad, down->cols_pad, inter, sel, w, slots, act, out, S);
-    qmv_status s = qmv::check_launch("moe kernels");
+    const qmv_status s = launch_ffn(gate, up, down, sel, w, slots, x, out, act, status, cs);
     cudaFreeAsync(act, cs);
     return s;
 }
@@ -366,8 +944,9 @@ extern "C" qmv_status moe_ffn_q8row(const qmv_weights* gate, const qmv_weights* 
 // that hand all device memory to their own allocator at start-up and refuse
 // allocations afterwards, and plugins loaded into such engines.  For them the
 // activation scratch of the two FFN kernels lives in the fixed array below.
-// Every GPU that loads this library holds it (256 KiB) until the process
-// exits; calls with slots * inter above its size are rejected.
+// Every GPU that loads this library holds it (256 KiB plus the row padding
+// of 64 slots) until the process exits; calls with slots * inter above
+// 65536 are rejected.
 //
 // All calls on a device share the array and it keeps the last call's
 // contents; nothing has to start at zero, because the gate/up kernel writes
@@ -380,9 +959,9 @@ extern "C" qmv_status moe_ffn_q8row(const qmv_weights* gate, const qmv_weights* 
 // device current, by the first call made on the device.  That first call
 // should come before any stream capture.
 // ---------------------------------------------------------------------------
-#include <mutex>
 
-constexpr int64_t kStaticActFloats = 1 << 16;   // slots * inter <= 65536
+constexpr int64_t kStaticActMax = 1 << 16;                 // slots * inter <= 65536
+constexpr int64_t kStaticActFloats = kStaticActMax + 3 * 64;   // + row padding to a multiple of 4
 static __device__ __align__(256) float g_static_act[kStaticActFloats];
 
 namespace {
@@ -415,34 +994,15 @@ qmv_status static_act_address(float** out) {
 extern "C" qmv_status moe_ffn_q8row_static(const qmv_weights* gate, const qmv_weights* up,
                                            const qmv_weights* down, const int32_t* sel, const float* w,
                                            int slots, const float* x, float* out, qmv_stream st) {
-    QMV_REQUIRE(gate && up && down && sel && w && x && out, QMV_ERR_INVALID_ARG,
-                "moe_ffn_q8row_static: null argument");
-    QMV_REQUIRE(gate->format == QMV_FMT_Q8ROW && up->format == QMV_FMT_Q8ROW && down->format == QMV_FMT_Q8ROW,
-                QMV_ERR_UNSUPPORTED, "moe_ffn_q8row_static: handles must be q8_row");
-    QMV_REQUIRE(slots >= 1 && slots <= 64, QMV_ERR_INVALID_ARG, "moe_ffn_q8row_static: need 1 <= slots <= 64");
-    const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
-    QMV_REQUIRE(up->experts == E && up->rows == inter && up->cols == hidden && down->experts == E &&
-                    down->rows == hidden && down->cols == inter,
-                QMV_ERR_INVALID_ARG, "moe_ffn_q8row_static: gate/up [E][inter][hidden] and down [E][hidden][inter] "
-                                     "shapes disagree");
-    QMV_REQUIRE((int64_t)slots * inter <= kStaticActFloats, QMV_ERR_UNSUPPORTED,
+    const qmv_status a = check_ffn_args("moe_ffn_q8row_static", gate, up, down, sel, w, slots, x, out);
+    if (a != QMV_OK) return a;
+    QMV_REQUIRE((int64_t)slots * gate->rows <= kStaticActMax, QMV_ERR_UNSUPPORTED,
                 "moe_ffn_q8row_static: slots * inter = %lld exceeds the fixed scratch of %lld floats",
-                (long long)((int64_t)slots * inter), (long long)kStaticActFloats);
-    QMV_REQUIRE(qmv::aligned16(x) && qmv::aligned16(out), QMV_ERR_INVALID_ARG,
-                "moe_ffn_q8row_static: x and out must be 16-byte aligned");
+                (long long)((int64_t)slots * gate->rows), (long long)kStaticActMax);
     int* status = qmv::device_status();
     QMV_REQUIRE(status, QMV_ERR_CUDA, "moe_ffn_q8row_static: no CUDA device");
     float* act = nullptr;
     const qmv_status sa = static_act_address(&act);
     if (sa != QMV_OK) return sa;
-    cudaStream_t cs = (cudaStream_t)st;
-    const dim3 g1((unsigned)(((inter + 3) / 4 + kWarps - 1) / kWarps), (unsigned)slots);
-    moe_gate_up_kernel<<<g1, kThreads, 0, cs>>>(gate->q, gate->rs, up->q, up->rs, E, inter, gate->rows_pad,
-                                                gate->cols_pad, hidden, sel, x, act, status);
-    const int S = slots >= 4 ? 4 : slots >= 2 ? 2 : 1;
-    const int gpc = kWarps / S;
-    const int64_t n_rg = (hidden + 3) / 4;
-    moe_down_kernel<<<(unsigned)((n_rg + gpc - 1) / gpc), kThreads, 0, cs>>>(
-        down->q, down->rs, E, hidden, down->rows_pad, down->cols_pad, inter, sel, w, slots, act, out, S);
-    return qmv::check_launch("moe_ffn_q8row_static kernels");
+    return launch_ffn(gate, up, down, sel, w, slots, x, out, act, status, (cudaStream_t)st);
 }

@@ -16,9 +16,19 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
     return v;
 }
 
-// Activations are re-read by every warp: keep them in L1.
+// Asks L2 to fetch [p, p + bytes) from HBM (no data comes to the SM);
+// p 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Activations are re-read by every warp: keep them in L1.  They may be the
+// output of the previous kernel in the stream, which can still be running
+// while this one starts (programmatic dependent launch), so they are read
+// after pdl_wait() with ordinary coherent loads, never the non-coherent
+// read-only path.
 __device__ __forceinline__ float4 ld_act_f4(const float* p) {
-    return __ldg(reinterpret_cast<const float4*>(p));
+    return __ldca(reinterpret_cast<const float4*>(p));
 }
 
 // Exact int8 -> f32 without the (quarter-rate) integer-to-float converter:
@@ -51,11 +61,16 @@ __device__ __forceinline__ void q8_chunk_fma(const uint4 w, const float4 x, floa
     }
 }
 
-// Activation float4 of lane `lane` for 128-column block `blk`; zero past `cols`.
+// Activation float4 of lane `lane` for 128-column block `blk`; zero past
+// `cols` (x 16-byte aligned; nothing at or past x[cols] is read).
 __device__ __forceinline__ float4 act_for_block(const float* x, int64_t blk, int lane, int64_t cols) {
     const int64_t c = blk * 128 + lane * 4;
-    if (c < cols) return ld_act_f4(x + c);
-    return make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c + 4 <= cols) return ld_act_f4(x + c);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < cols) v.x = __ldca(x + c);
+    if (c + 1 < cols) v.y = __ldca(x + c + 1);
+    if (c + 2 < cols) v.z = __ldca(x + c + 2);
+    return v;
 }
 
 // Sum of a float over the 32 lanes, result in every lane.
@@ -65,18 +80,38 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Dot products of the 4 rows of row group `rg` (base: packed codes of the
-// matrix) with x over blocks [b0, b1).  Returns the 4 per-lane partials.
+// Codes of blocks [b0, b0 + U) of row group `rg` (zero at and past b1): the
+// batch a kernel loads before its dependency wait.
 template <int U>
-__device__ __forceinline__ void q8_rowgroup_dot(const int8_t* __restrict__ qbase, int64_t cols_pad,
-                                                int64_t rg, int64_t b0, int64_t b1,
-                                                const float* __restrict__ x, int64_t cols, int lane,
-                                                float out[4]) {
+__device__ __forceinline__ void q8_first_codes(uint4 (&w)[U], const int8_t* __restrict__ qbase, int64_t cols_pad,
+                                               int64_t rg, int64_t b0, int64_t b1, int lane) {
+    const int8_t* p = qbase + rg * 4 * cols_pad + lane * 16;
+#pragma unroll
+    for (int u = 0; u < U; ++u) w[u] = b0 + u < b1 ? ld_stream_u4(p + (b0 + u) * 512) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Dot products of the 4 rows of row group `rg` (qbase: packed codes of the
+// matrix) with x over blocks [b0, b1), when the codes of [b0, b0 + U) are
+// already in w0 (from q8_first_codes; zero codes contribute exactly 0).
+// Returns the 4 per-lane partials.
+template <int U>
+__device__ __forceinline__ void q8_rowgroup_dot_from(const uint4 (&w0)[U], const int8_t* __restrict__ qbase,
+                                                     int64_t cols_pad, int64_t rg, int64_t b0, int64_t b1,
+                                                     const float* __restrict__ x, int64_t cols, int lane,
+                                                     float out[4]) {
     float2 acc[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[r] = make_float2(0.f, 0.f);
+    {
+        float4 xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            xv[u] = b0 + u < b1 ? act_for_block(x, b0 + u, lane, cols) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < U; ++u) q8_chunk_fma(w0[u], xv[u], acc);
+    }
     const int8_t* p = qbase + rg * 4 * cols_pad + lane * 16;
-    int64_t b = b0;
+    int64_t b = b0 + U;
     for (; b + U <= b1; b += U) {
         uint4 w[U];
         float4 xv[U];

@@ -72,6 +72,47 @@ enum : int {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The decode kernels are launched so that
+// they may start while the previous kernel in the stream is still running;
+// each one executes pdl_wait() before it reads any input that the previous
+// kernel may write (activations, selections, router weights) or writes any
+// output, and may read only the packed weights before that.  Right after its
+// own pdl_wait() it calls pdl_launch_dependents(), so the next kernel can
+// become resident: anything that kernel reads before its own wait (weights,
+// or the inputs of the call it belongs to, which were complete before this
+// call's first wait returned) is then already final.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` as a programmatic dependent launch: it may start while
+// the previous kernel in the stream is still running, and must execute
+// griddepcontrol.wait before it reads anything that kernel may produce.
+template <typename... KArgs, typename... Args>
+qmv_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(QMV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return QMV_OK;
+}
+
+
 }  // namespace qmv
 
 // Validation helpers for the entry points.

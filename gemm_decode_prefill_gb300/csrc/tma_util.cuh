@@ -103,28 +103,4 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// Launches `kernel` as a programmatic dependent launch: it may start while
-// the previous kernel in the stream is still running, and must execute
-// griddepcontrol.wait before it reads anything that kernel may produce.
-template <typename... KArgs, typename... Args>
-qmv_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                      Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(QMV_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
-    }
-    return QMV_OK;
-}
-
 }  // namespace qmv

@@ -30,6 +30,14 @@
  *    them with qmv_weights_free() after all work that reads them is done.
  *  - Thread safety: calls that read a handle may run concurrently; packing
  *    and freeing a handle need external ordering.
+ *  - The decode kernels (qmv_q8row, moe_select_topk, moe_ffn_q8row*) are
+ *    programmatic dependent launches: each may start while the previous
+ *    kernel in `st` is still running, and before waiting for it reads only
+ *    packed weights (and, in the down kernel of the expert FFN, sel and w,
+ *    which the FFN's own first kernel has already waited for).  Activations,
+ *    selections and outputs are read or written only after that wait, so
+ *    stream order holds as usual.  Packed weights must not be written by
+ *    the kernel that precedes such a call.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -197,7 +205,8 @@ QMV_API qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
  * is a library convenience, not part of the method.
  *   Same arguments, results and errors as moe_ffn_q8row, plus:
  *   slots * inter <= 65536, else QMV_ERR_UNSUPPORTED.
- * The activation scratch is a fixed 256 KiB array in device memory that
+ * The activation scratch is a fixed array of 256 KiB (plus 768 bytes of
+ * row padding) in device memory that
  * every GPU loading the library holds until exit; the call makes no
  * allocation.  All calls on a device share it, so calls whose GPU work
  * overlaps (unordered streams) race: order them.  The first call on a device

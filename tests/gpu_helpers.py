@@ -38,3 +38,20 @@ def assert_within(y, y_ref, mag, tol, what, floor=0.0):
 def d16(d_bits: np.ndarray) -> torch.Tensor:
     """f16 bit patterns (uint16 numpy) as a CUDA int16 tensor for the binding."""
     return torch.from_numpy(np.ascontiguousarray(d_bits).view(np.int16)).cuda()
+
+
+def moe_bound(m, sel, w, parts):
+    """Composite bound: the GEMV bound on each stage, propagated through
+    silu(g)*u and the weighted down projection, times 4."""
+    g, u, act = parts["g"], parts["u"], parts["act"]
+    x = np.abs(m.x.astype(np.float64))
+    tol = TOL_GEMV * parts["mag"]
+    for s, e in enumerate(sel):
+        mag_g = np.abs(m.grs[e].astype(np.float64)) * (np.abs(m.gq[e].astype(np.float64)) @ x)
+        mag_u = np.abs(m.urs[e].astype(np.float64)) * (np.abs(m.uq[e].astype(np.float64)) @ x)
+        sig = 1.0 / (1.0 + np.exp(-g[s]))
+        dsilu = np.abs(sig * (1.0 + g[s] * (1.0 - sig)))
+        dact = (dsilu * np.abs(u[s]) * TOL_GEMV * mag_g + np.abs(g[s] * sig) * TOL_GEMV * mag_u
+                + 1e-6 * np.abs(act[s]))
+        tol = tol + abs(w[s]) * np.abs(m.drs[e].astype(np.float64)) * (np.abs(m.dq[e].astype(np.float64)) @ dact)
+    return 4.0 * tol

@@ -1,0 +1,186 @@
+"""Back-to-back decode calls on one stream.
+
+The decode kernels are programmatic dependent launches: each may start, and
+load its weights, before the previous kernel in the stream has finished, and
+waits for that kernel before it touches activations or outputs.  A call that
+reads the previous call's output, or overwrites the previous call's input,
+must therefore give exactly what the same calls give when the host
+synchronises after every call.  Every kernel here is deterministic, so the
+comparison is bit for bit; each stage is also checked against the oracle on
+the input that stage actually read."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gemm_decode_prefill_gb300 import synth
+from gpu_helpers import TOL_GEMV, TOL_ROUTER_W, assert_within, dev, host, moe_bound
+
+pytestmark = pytest.mark.gpu
+
+N = 2048
+
+
+@pytest.fixture(scope="module")
+def qmv():
+    from gemm_decode_prefill_gb300 import qmv as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def square(qmv):
+    mats = []
+    for i in range(4):
+        q, rs, _ = synth.q8_inputs(N, N, 300 + i)
+        mats.append((q, rs, qmv.qmv_pack_q8row(dev(q), dev(rs))))
+    torch.cuda.synchronize()
+    return mats
+
+
+def _x0():
+    return synth.rng(299).standard_normal(N).astype(np.float32)
+
+
+def _chain(qmv, square, sync):
+    """x -> W0 x -> W1 (W0 x) -> ..., every stage into its own buffer."""
+    s = torch.cuda.Stream()
+    bufs = [dev(_x0())] + [torch.full((N,), float("nan"), device="cuda") for _ in square]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i, (_, _, w) in enumerate(square):
+            qmv.qmv_q8row(w, bufs[i], bufs[i + 1], stream=s)
+            if sync:
+                s.synchronize()
+    torch.cuda.synchronize()
+    return [host(b) for b in bufs]
+
+
+def test_q8_chain_reads_previous_output(qmv, square):
+    fast, slow = _chain(qmv, square, False), _chain(qmv, square, True)
+    for i in range(1, len(fast)):
+        assert np.array_equal(fast[i], slow[i]), f"stage {i} differs from the synchronised run"
+        q, rs, _ = square[i - 1]
+        y_ref, mag = oracle.q8row(q, rs, fast[i - 1], with_mag=True)
+        assert_within(fast[i], y_ref, mag, TOL_GEMV, f"chain stage {i}")
+
+
+def test_q8_ping_pong_overwrites_input(qmv, square):
+    """Stage k reads buffer A and writes B, stage k+1 reads B and writes A."""
+    def run(sync):
+        s = torch.cuda.Stream()
+        a, b = dev(_x0()), torch.empty(N, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for k in range(6):
+                src, dst = (a, b) if k % 2 == 0 else (b, a)
+                qmv.qmv_q8row(square[k % 2][2], src, dst, stream=s)
+                if sync:
+                    s.synchronize()
+        torch.cuda.synchronize()
+        return host(a), host(b)
+    fa, fb = run(False)
+    sa, sb = run(True)
+    assert np.array_equal(fa, sa) and np.array_equal(fb, sb)
+    assert np.isfinite(fa).all()
+
+
+def test_q8_chain_in_a_cuda_graph(qmv, square):
+    s = torch.cuda.Stream()
+    bufs = [dev(_x0())] + [torch.empty(N, device="cuda") for _ in square]
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        qmv.qmv_q8row(square[0][2], bufs[0], bufs[1], stream=s)   # first-use set-up outside the capture
+        s.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for i, (_, _, w) in enumerate(square):
+                qmv.qmv_q8row(w, bufs[i], bufs[i + 1], stream=s)
+    expected = _chain(qmv, square, True)
+    for _ in range(2):
+        for b in bufs[1:]:
+            b.fill_(float("nan"))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.replay()
+        got = [host(b) for b in bufs]
+        for i in range(1, len(got)):
+            assert np.array_equal(got[i], expected[i]), f"graph replay stage {i}"
+
+
+H, I, E, K, STEPS = 512, 256, 32, 4, 6
+
+
+def _pack(qmv, m):
+    w = (qmv.qmv_pack_q8row(dev(m.gq), dev(m.grs)), qmv.qmv_pack_q8row(dev(m.uq), dev(m.urs)),
+         qmv.qmv_pack_q8row(dev(m.dq), dev(m.drs)))
+    torch.cuda.synchronize()
+    return m, w
+
+
+@pytest.fixture(scope="module")
+def moe(qmv):
+    return _pack(qmv, synth.moe_inputs(E, H, I, seed=310))
+
+
+@pytest.fixture(scope="module")
+def moe_chain(qmv):
+    """The same experts with the down scales divided by the rms of the first
+    step's output: out grows like x^2, so without this a chain of steps
+    overflows f32 within a few steps."""
+    m = synth.moe_inputs(E, H, I, seed=310)
+    bank = synth.logit_bank(E, STEPS, 310)
+    sel, w = oracle.select(bank[0], K, True, sgw=m.sgw, x=m.x)
+    out = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel, w, m.x)
+    rms = float(np.sqrt(np.mean(np.square(out))))
+    return _pack(qmv, dataclasses.replace(m, drs=(m.drs / rms).astype(np.float32)))
+
+
+def _moe_steps(qmv, moe, sync, static, chain_x):
+    """STEPS router + FFN steps with shared sel / w (and act scratch), each
+    with its own logits; with chain_x, step i+1 takes step i's output as x."""
+    m, (gate, up, down) = moe
+    bank = dev(synth.logit_bank(E, STEPS, 310))
+    sgw = dev(m.sgw)
+    xs = [dev(m.x)] + [torch.full((H,), float("nan"), device="cuda") for _ in range(STEPS)]
+    sel = torch.empty(K + 1, dtype=torch.int32, device="cuda")
+    w = torch.empty(K + 1, device="cuda")
+    sels, ws = [], []
+    ffn = qmv.moe_ffn_q8row_static if static else qmv.moe_ffn_q8row
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for i in range(STEPS):
+            x = xs[i] if chain_x else xs[0]
+            qmv.moe_select_topk(bank[i], K, True, sg_w=sgw, x=x, sel=sel, w=w, stream=s)
+            ffn(gate, up, down, sel, w, x, xs[i + 1], stream=s)
+            if sync:
+                s.synchronize()
+                sels.append(host(sel).copy())
+                ws.append(host(w).copy())
+    torch.cuda.synchronize()
+    return [host(t) for t in xs], sels, ws
+
+
+@pytest.mark.parametrize("chain_x", [False, True])
+def test_moe_steps_back_to_back(qmv, moe, moe_chain, chain_x):
+    moe = moe_chain if chain_x else moe
+    fast, _, _ = _moe_steps(qmv, moe, False, False, chain_x)
+    fast_static, _, _ = _moe_steps(qmv, moe, False, True, chain_x)
+    slow, sels, ws = _moe_steps(qmv, moe, True, False, chain_x)
+    assert all(np.isfinite(t).all() for t in slow)
+    for i in range(1, STEPS + 1):
+        assert np.array_equal(fast[i], slow[i]), f"step {i - 1} differs from the synchronised run"
+        assert np.array_equal(fast_static[i], slow[i]), f"static step {i - 1} differs"
+    m, _ = moe
+    bank = synth.logit_bank(E, STEPS, 310)
+    for i in (0, STEPS - 1):
+        x = slow[i] if chain_x else m.x
+        sel_ref, w_ref = oracle.select(bank[i], K, True, sgw=m.sgw, x=x)
+        assert sels[i].tolist() == sel_ref.tolist()
+        np.testing.assert_allclose(ws[i].astype(np.float64), w_ref, rtol=TOL_ROUTER_W, atol=0)
+        mi = dataclasses.replace(m, x=np.asarray(x, np.float32))
+        out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel_ref, w_ref, mi.x,
+                                        with_parts=True)
+        assert_within(slow[i + 1], out_ref, moe_bound(mi, sel_ref, w_ref, parts), 1.0, f"moe step {i}")

@@ -18,7 +18,11 @@ def qmv():
 
 # ------------------------------------------------------------------ q8_row
 
-Q8_SHAPES = [(1, 16), (5, 48), (37, 128), (64, 144), (300, 640), (129, 1040), (1000, 4096), (4096, 4096)]
+# (40, 24576): a 4-row group of exactly 96 KB, the largest the shared-memory
+# kernel stages; (13, 24592) and (8192, 4096) (32 MB of codes) go to the
+# register-streaming kernel.
+Q8_SHAPES = [(1, 16), (5, 48), (37, 128), (64, 144), (2000, 272), (300, 640), (129, 1040), (1000, 4096),
+             (4099, 2048), (4096, 4096), (8192, 4096), (40, 24576), (13, 24592)]
 
 
 @pytest.mark.parametrize("rows,cols", Q8_SHAPES)

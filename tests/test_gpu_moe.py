@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from gemm_decode_prefill_gb300 import synth
-from gpu_helpers import TOL_GEMV, TOL_ROUTER_W, assert_within, dev, host
+from gpu_helpers import TOL_GEMV, TOL_ROUTER_W, assert_within, dev, host, moe_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -69,23 +69,6 @@ def _pack_moe(qmv, m):
             qmv.qmv_pack_q8row(dev(m.dq), dev(m.drs)))
 
 
-def _moe_bound(m, sel, w, parts):
-    """Composite bound: the GEMV bound on each stage, propagated through
-    silu(g)*u and the weighted down projection, times 4."""
-    g, u, act = parts["g"], parts["u"], parts["act"]
-    x = np.abs(m.x.astype(np.float64))
-    tol = TOL_GEMV * parts["mag"]
-    for s, e in enumerate(sel):
-        mag_g = np.abs(m.grs[e].astype(np.float64)) * (np.abs(m.gq[e].astype(np.float64)) @ x)
-        mag_u = np.abs(m.urs[e].astype(np.float64)) * (np.abs(m.uq[e].astype(np.float64)) @ x)
-        sig = 1.0 / (1.0 + np.exp(-g[s]))
-        dsilu = np.abs(sig * (1.0 + g[s] * (1.0 - sig)))
-        dact = (dsilu * np.abs(u[s]) * TOL_GEMV * mag_g + np.abs(g[s] * sig) * TOL_GEMV * mag_u
-                + 1e-6 * np.abs(act[s]))
-        tol = tol + abs(w[s]) * np.abs(m.drs[e].astype(np.float64)) * (np.abs(m.dq[e].astype(np.float64)) @ dact)
-    return 4.0 * tol
-
-
 def _run_step(qmv, m, k, renorm):
     gate, up, down = _pack_moe(qmv, m)
     sel, w = qmv.moe_select_topk(dev(m.logits), k, renorm, sg_w=dev(m.sgw), x=dev(m.x))
@@ -102,7 +85,7 @@ def test_moe_step_matches_oracle(qmv, n_exp, hidden, inter, k):
     np.testing.assert_allclose(w.astype(np.float64), w_ref, rtol=TOL_ROUTER_W, atol=0)
     out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel_ref, w_ref, m.x,
                                     with_parts=True)
-    bound = _moe_bound(m, sel_ref, w_ref, parts)
+    bound = moe_bound(m, sel_ref, w_ref, parts)
     assert_within(out, out_ref, bound, 1.0, f"moe {n_exp}x{hidden}x{inter} k={k}")
 
 
@@ -115,7 +98,7 @@ def test_moe_ffn_given_selection_matches_oracle(qmv):
     out = host(qmv.moe_ffn_q8row(gate, up, down, dev(sel), dev(w), dev(m.x)))
     out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel, w.astype(np.float64), m.x,
                                     with_parts=True)
-    assert_within(out, out_ref, _moe_bound(m, sel, w, parts), 1.0, "moe ffn given selection")
+    assert_within(out, out_ref, moe_bound(m, sel, w, parts), 1.0, "moe ffn given selection")
 
 
 def test_moe_bad_expert_sets_device_status(qmv):
