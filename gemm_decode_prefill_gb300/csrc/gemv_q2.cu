@@ -15,7 +15,10 @@
 //     (q-1)*x is formed without rounding and summed in fp32;
 //   * the per-group scale d (f16 -> f32, exact) multiplies the fp32 group sum.
 // The K range is split across the warps of a CTA; partial sums are reduced
-// in shared memory in a fixed order (deterministic).
+// in shared memory in a fixed order (deterministic).  The persistent kernel
+// is a programmatic dependent launch: its producer warp starts fetching the
+// constant codes and scales while the previous kernel in the stream is still
+// running, and the consumers wait for that kernel before reading x.
 #include "tma_util.cuh"
 
 namespace {
@@ -652,9 +655,13 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
     if (warp == kV3Warps) {
         // ---------------- producer ----------------
         if (lane == 0) {
+            // the codes and scales are constant: the first round is fetched
+            // before the consumers' dependency wait (programmatic launch)
             int64_t issued_rounds = 0;
             for (int64_t r = 0; r < rounds; ++r) {
                 if (r > 0 && !qmv::mbar_wait(&rdone[0], (uint32_t)(r - 1) & 1u, abort, status)) break;
+                // one round done: the consumers have passed their wait
+                if (r == 1) qmv::pdl_launch_dependents();
                 for (int i = 0; i < TR; ++i) {
                     const int64_t t = t0 + r * TR + i;
                     if (t >= t1) break;
@@ -675,6 +682,10 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
         return;
     }
 
+    // x (and y) may belong to the previous kernel in the stream
+    qmv::pdl_wait();
+    qmv::pdl_launch_dependents();
+
     // ---------------- activation split into B fragments ----------------
     // Layout per chunk: [k-step pair j][13 slots] uint4; slot l (< 12) holds
     // lane l's registers for k-steps 2j and 2j+1, slot 12 is zero, so the
@@ -692,8 +703,8 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
             if (e < n) {
                 const int64_t k0 = 16 * (int64_t)(e >> 2) + 2 * (e & 3);
                 if (k0 < cols) {   // cols % 64 == 0: then k0 + 9 < cols too
-                    lo[u] = __ldg(reinterpret_cast<const float2*>(x + k0));
-                    hi[u] = __ldg(reinterpret_cast<const float2*>(x + k0 + 8));
+                    lo[u] = __ldca(reinterpret_cast<const float2*>(x + k0));
+                    hi[u] = __ldca(reinterpret_cast<const float2*>(x + k0 + 8));
                 }
             }
         }
@@ -830,10 +841,8 @@ qmv_status launch_q2_v3(const qmv_weights* w, const Q2PlanV3& p, const float* x,
     const int64_t n_tiles = w->rows_pad / 16;
     int64_t grid = qmv::sm_count();
     if (grid > n_tiles) grid = n_tiles;
-    q2_gemv_v3_kernel<G><<<(unsigned)grid, kV3Threads, p.smem, st>>>(w->codes, w->d, x, y, w->rows, w->cols, KC, p.TR,
-                                                                     p.WPT, p.tile_bytes, p.code_bytes, n_tiles,
-                                                                     status);
-    return qmv::check_launch("q2_gemv_v3_kernel");
+    return qmv::launch_pdl(q2_gemv_v3_kernel<G>, dim3((unsigned)grid), dim3(kV3Threads), p.smem, st, w->codes, w->d, x,
+                           y, w->rows, w->cols, KC, p.TR, p.WPT, p.tile_bytes, p.code_bytes, n_tiles, status);
 }
 
 template <int G>
