@@ -586,6 +586,44 @@ def run_reference(args, rank, world):
             "impl": "reference"}
 
 
+def run_rows_only(launches: int = 0):
+    """The q8 GEMV, prefill GEMM and MoE rows alone (no Q2 step, no CPU leg);
+    with launches > 0, only that many untimed calls of two of them."""
+    import torch
+    from gemm_decode_prefill_gb300 import qmv, synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream()
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    if launches <= 0:
+        return {"rows": measure_rows(qmv, synth, up, dev, stream, load_peaks()), "impl": "ours"}
+    cfg = synth.WORKLOADS["q8_gemv_4096x4096"]
+    q, rs, xs = synth.q8_inputs(cfg["rows"], cfg["cols"], cfg["seed"])
+    qd, rd = up(q), up(rs)
+    ws = [qmv.qmv_pack_q8row(qd, rd, stream=stream) for _ in range(16)]
+    xd, y = up(xs), torch.empty(cfg["rows"], device=dev)
+    for i in range(launches):
+        qmv.qmv_q8row(ws[i % 16], xd, y, stream=stream)
+    cfg = synth.WORKLOADS["moe_decode_h2048_e128_k8"]
+    m = synth.moe_inputs(cfg["n_exp"], cfg["hidden"], cfg["inter"], cfg["seed"])
+    gate = qmv.qmv_pack_q8row(up(m.gq), up(m.grs), stream=stream)
+    upw = qmv.qmv_pack_q8row(up(m.uq), up(m.urs), stream=stream)
+    down = qmv.qmv_pack_q8row(up(m.dq), up(m.drs), stream=stream)
+    bank = up(synth.logit_bank(cfg["n_exp"], 64, cfg["seed"]))
+    xm, sgw = up(m.x), up(m.sgw)
+    sel = torch.empty(cfg["top_k"] + 1, dtype=torch.int32, device=dev)
+    wsel = torch.empty(cfg["top_k"] + 1, device=dev)
+    out = torch.empty(cfg["hidden"], device=dev)
+    for i in range(launches):
+        qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xm, sel=sel, w=wsel,
+                            stream=stream)
+        qmv.moe_ffn_q8row(gate, upw, down, sel, wsel, xm, out, stream=stream)
+    torch.cuda.synchronize()
+    return {"rows": "untimed", "launches": launches, "impl": "ours"}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -594,6 +632,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--rows-only", action="store_true",
+                    help="only the other workloads (q8 GEMVs, prefill GEMM, MoE step), one JSON line; for profiling")
+    ap.add_argument("--launches", type=int, default=0,
+                    help="with --rows-only: just N untimed eager calls of the q8 4096x4096 GEMV and the MoE step "
+                         "(a small program for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args(argv)
@@ -603,6 +646,8 @@ def main(argv=None):
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
         line = run_reference(args, rank, world)
+    elif args.rows_only:
+        line = run_rows_only(args.launches)
     else:
         rank, world, local = dist_setup()
         line = run_ours(args, rank, world, local)
