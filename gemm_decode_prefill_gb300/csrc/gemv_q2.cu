@@ -607,6 +607,7 @@ Q2PlanV3 q2_plan_v3(int KC) {
     const size_t fixed = (size_t)KC * 52 * sizeof(uint4) + kV3Warps * 32 * sizeof(float) +
                          (2 * kV3MaxTR + 2) * sizeof(uint64_t) + 16 + 128;
     p.ok = false;
+    if (KC > kTmaMaxChunks) return p;   // the activation prologue covers at most kTmaMaxChunks chunks
     for (int tr = kV3MaxTR; tr >= 1; tr >>= 1) {
         if (fixed + (size_t)tr * p.tile_bytes <= limit && KC >= kV3Warps / tr) {
             p.TR = tr;
