@@ -503,16 +503,16 @@ def measure_rows(qmv, synth, up, dev, stream, peaks):
     wsel = torch.empty(cfg["top_k"] + 1, device=dev)
     outv = torch.empty(cfg["hidden"], device=dev)
 
-    def moe_step(i):
-        qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xd, sel=sel, w=wsel,
-                            stream=stream)
-        qmv.moe_ffn_q8row(gate, upw, down, sel, wsel, xd, outv, stream=stream)
+    def moe_step(i):   # router select + expert FFN, one call
+        qmv.moe_step_q8row(bank[i % 64], cfg["top_k"], cfg["renorm"], gate, upw, down, xd, sg_w=sgw, sel=sel,
+                           w=wsel, out=outv, stream=stream)
 
     t = kernel_time(moe_step, 64, stream)
     ts = kernel_time(lambda i: qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xd,
                                                     sel=sel, w=wsel, stream=stream), 64, stream)
     b = moe_bytes(cfg["top_k"] + 1, cfg["hidden"], cfg["inter"])
-    out["moe_decode_h2048_e128_k8"] = {"kernels": "moe_select_kernel, moe_gate_up_smem_kernel, moe_down_smem_kernel",
+    out["moe_decode_h2048_e128_k8"] = {"kernels": "moe_select_kernel, moe_gate_up_smem_kernel, moe_down_smem_kernel "
+                                                  "(moe_step_q8row)",
                                        "us_per_step": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
                                        "frac_hbm": round(b / t / 1e9 / hbm, 4), "bytes": b,
                                        "select_us": round(ts * 1e6, 3),
@@ -617,9 +617,8 @@ def run_rows_only(launches: int = 0):
     wsel = torch.empty(cfg["top_k"] + 1, device=dev)
     out = torch.empty(cfg["hidden"], device=dev)
     for i in range(launches):
-        qmv.moe_select_topk(bank[i % 64], cfg["top_k"], cfg["renorm"], sg_w=sgw, x=xm, sel=sel, w=wsel,
-                            stream=stream)
-        qmv.moe_ffn_q8row(gate, upw, down, sel, wsel, xm, out, stream=stream)
+        qmv.moe_step_q8row(bank[i % 64], cfg["top_k"], cfg["renorm"], gate, upw, down, xm, sg_w=sgw, sel=sel,
+                           w=wsel, out=out, stream=stream)
     torch.cuda.synchronize()
     return {"rows": "untimed", "launches": launches, "impl": "ours"}
 

@@ -731,51 +731,65 @@ __global__ void __launch_bounds__(kThreads) moe_down_smem_kernel(
     const int nblk = (int)(cols_pad / 128);
     const int U = slots * Rc;
 
-    // Before the dependency wait.  sel and w were final before the gate/up
-    // kernel of this call passed its own wait, and this grid launched only
-    // after that.
-    if (threadIdx.x < slots) {
-        const int e = __ldcg(sel + threadIdx.x);
-        s_e[threadIdx.x] = e >= 0 && e < n_experts ? e : -1;
-    }
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < slots; ++s) qmv::mbar_init(&bar[s], 1);
         qmv::mbar_fence_init();
     }
     for (int i = threadIdx.x; i < U * kWarps * 4; i += kThreads) (&part[0][0][0])[i] = 0.f;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < slots; ++s) {
-            const int e = s_e[s];
-            if (e < 0) {   // reported by the gate/up kernel; nothing to fetch
-                qmv::mbar_arrive(&bar[s]);
-                continue;
-            }
-            const int64_t bytes = Rc * rgb;
-            qmv::mbar_arrive_tx(&bar[s], (uint32_t)bytes);
-            const int8_t* src = dq + (int64_t)e * rows_pad * cols_pad + g0 * rgb;
-            for (int64_t o = 0; o < bytes; o += 32768)
-                qmv::bulk_g2s(smc + (int64_t)s * Rc * rgb + o, src + o,
-                              (uint32_t)(bytes - o < 32768 ? bytes - o : 32768), &bar[s]);
+    // Before the dependency wait: the experts, their codes (bulk copies), row
+    // scales and router weights.  sel and w were final before the gate/up
+    // kernel of this call passed its own wait, and this grid launched only
+    // after that.
+    {
+        if (threadIdx.x < slots) {
+            const int e = __ldcg(sel + threadIdx.x);
+            s_e[threadIdx.x] = e >= 0 && e < n_experts ? e : -1;
         }
-    }
-    for (int t = threadIdx.x; t < U * 4; t += kThreads) {
-        const int s = t / (Rc * 4), j = t - s * Rc * 4;
-        const int e = s_e[s];
-        const int64_t row = g0 * 4 + j;
-        s_f[t] = e >= 0 && row < hidden ? __ldcg(wsel + s) * drs[(int64_t)e * rows_pad + row] : 0.f;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < slots; ++s) {
+                const int e = s_e[s];
+                if (e < 0) {   // reported by the gate/up kernel; nothing to fetch
+                    qmv::mbar_arrive(&bar[s]);
+                    continue;
+                }
+                const int64_t bytes = Rc * rgb;
+                qmv::mbar_arrive_tx(&bar[s], (uint32_t)bytes);
+                const int8_t* src = dq + (int64_t)e * rows_pad * cols_pad + g0 * rgb;
+                for (int64_t o = 0; o < bytes; o += 32768)
+                    qmv::bulk_g2s(smc + (int64_t)s * Rc * rgb + o, src + o,
+                                  (uint32_t)(bytes - o < 32768 ? bytes - o : 32768), &bar[s]);
+            }
+        }
+        for (int t = threadIdx.x; t < U * 4; t += kThreads) {
+            const int s = t / (Rc * 4), j = t - s * Rc * 4;
+            const int e = s_e[s];
+            const int64_t row = g0 * 4 + j;
+            s_f[t] = e >= 0 && row < hidden ? __ldcg(wsel + s) * drs[(int64_t)e * rows_pad + row] : 0.f;
+        }
     }
     qmv::pdl_wait();
     qmv::pdl_launch_dependents();
-    // act of every slot, zero-padded to cols_pad, loaded once per CTA
+    // act of every slot, zero-padded to cols_pad, loaded once per CTA: thread
+    // t stages column float4 t (t, t + kThreads, ...) of every slot, the
+    // loads of up to kActBatch slots issued before any store
     float4* as4 = reinterpret_cast<float4*>(smc + (int64_t)U * rgb);
-    stage_f4(as4, slots * nblk * 32, [&](int i) {
-        const int s = i / (nblk * 32);
-        const int64_t c = (int64_t)(i - s * nblk * 32) * 4;
-        return c < act_stride ? __ldcg(reinterpret_cast<const float4*>(act + (int64_t)s * act_stride + c))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    });
+    constexpr int kActBatch = 16;
+    for (int j = threadIdx.x; j < nblk * 32; j += kThreads) {
+        const int64_t c = 4 * (int64_t)j;
+        for (int s0 = 0; s0 < slots; s0 += kActBatch) {
+            float4 v[kActBatch];
+#pragma unroll
+            for (int q = 0; q < kActBatch; ++q)
+                v[q] = s0 + q < slots && c < act_stride
+                           ? __ldcg(reinterpret_cast<const float4*>(act + (int64_t)(s0 + q) * act_stride + c))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kActBatch; ++q)
+                if (s0 + q < slots) as4[(s0 + q) * nblk * 32 + j] = v[q];
+        }
+    }
     __syncthreads();
 
     int a, b;
@@ -842,12 +856,45 @@ qmv_status check_ffn_args(const char* fn, const qmv_weights* gate, const qmv_wei
 }
 
 // The two FFN launches; act: [slots][act_stride_of(inter)] floats, 16-byte aligned.
+// Row groups per CTA of the staged kernels (0: the shape is too wide to stage).
+struct FfnPlan {
+    int64_t gu_r, dn_r;
+};
+
+FfnPlan ffn_plan(const qmv_weights* gate, const qmv_weights* down, int slots) {
+    const int64_t sms = qmv::sm_count();
+    FfnPlan p{0, 0};
+    // gate/up: codes of gu_r row groups of both matrices, plus x (cols_pad
+    // floats = one row group's bytes); about three CTAs per SM
+    const int64_t gu_rgb = 4 * gate->cols_pad;
+    const int64_t n_rg_i = (gate->rows + 3) / 4;
+    int64_t gu_r = (kFfnSmem / gu_rgb - 1) / 2 < kGuMaxRG ? (kFfnSmem / gu_rgb - 1) / 2 : kGuMaxRG;
+    if (gu_r >= 1) {
+        const int64_t want = (slots * n_rg_i + 3 * sms - 1) / (3 * sms);
+        if (gu_r > want) gu_r = want < 1 ? 1 : want;
+        p.gu_r = gu_r;
+    }
+    // down: codes of dn_r row groups per slot, plus act (slots x cols_pad
+    // floats = one row group's bytes per slot); about two CTAs per SM
+    const int64_t n_rg = (down->rows + 3) / 4;
+    const int64_t dn_rgb = 4 * down->cols_pad;
+    int64_t dn_r = kFfnSmem / (slots * dn_rgb) - 1;
+    if (dn_r > kDnMaxUnits / slots) dn_r = kDnMaxUnits / slots;
+    if (dn_r >= 1) {
+        const int64_t want = (n_rg + 2 * sms - 1) / (2 * sms);
+        if (dn_r > want) dn_r = want < 1 ? 1 : want;
+        p.dn_r = dn_r;
+    }
+    return p;
+}
+
+// The two FFN launches; act: [slots][act_stride_of(inter)] floats, 16-byte
+// aligned.
 qmv_status launch_ffn(const qmv_weights* gate, const qmv_weights* up, const qmv_weights* down,
                       const int32_t* sel, const float* w, int slots, const float* x, float* out, float* act,
                       int* status, cudaStream_t cs) {
     const int64_t E = gate->experts, inter = gate->rows, hidden = gate->cols;
     const int64_t astride = act_stride_of(inter);
-    const int64_t sms = qmv::sm_count();
     static int configured[64] = {0};
     const int dev = qmv::current_device();
     if (dev >= 0 && dev < 64 && !configured[dev]) {
@@ -855,19 +902,16 @@ qmv_status launch_ffn(const qmv_weights* gate, const qmv_weights* up, const qmv_
         cudaFuncSetAttribute(moe_down_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFfnSmem);
         configured[dev] = 1;
     }
+    const FfnPlan plan = ffn_plan(gate, down, slots);
     qmv_status st;
-    // gate/up: about three staged CTAs per SM
-    const int64_t gu_rgb = 4 * gate->cols_pad;
     const int64_t n_rg_i = (inter + 3) / 4;
-    // codes of gu_r row groups of both matrices, plus x (cols_pad floats = one row group's bytes)
-    int64_t gu_r = (kFfnSmem / gu_rgb - 1) / 2 < kGuMaxRG ? (kFfnSmem / gu_rgb - 1) / 2 : kGuMaxRG;
-    if (gu_r >= 1) {
-        const int64_t want = (slots * n_rg_i + 3 * sms - 1) / (3 * sms);
-        if (gu_r > want) gu_r = want < 1 ? 1 : want;
-        const dim3 g1((unsigned)((n_rg_i + gu_r - 1) / gu_r), (unsigned)slots);
-        st = qmv::launch_pdl(moe_gate_up_smem_kernel, g1, dim3(kThreads), (size_t)((2 * gu_r + 1) * gu_rgb), cs, gate->q,
-                             gate->rs, up->q, up->rs, E, inter, gate->rows_pad, gate->cols_pad, hidden, (int)gu_r,
-                             down->q, down->rs, down->rows_pad, down->cols_pad, sel, x, act, astride, status);
+    if (plan.gu_r >= 1) {
+        const int64_t gu_rgb = 4 * gate->cols_pad;
+        const dim3 g1((unsigned)((n_rg_i + plan.gu_r - 1) / plan.gu_r), (unsigned)slots);
+        st = qmv::launch_pdl(moe_gate_up_smem_kernel, g1, dim3(kThreads), (size_t)((2 * plan.gu_r + 1) * gu_rgb), cs,
+                             gate->q, gate->rs, up->q, up->rs, E, inter, gate->rows_pad, gate->cols_pad, hidden,
+                             (int)plan.gu_r, down->q, down->rs, down->rows_pad, down->cols_pad, sel, x, act, astride,
+                             status);
     } else {
         const dim3 g1((unsigned)((n_rg_i + kWarps - 1) / kWarps), (unsigned)slots);
         if (gate->cols_pad <= kXSmemMax) {
@@ -881,18 +925,14 @@ qmv_status launch_ffn(const qmv_weights* gate, const qmv_weights* up, const qmv_
         }
     }
     if (st != QMV_OK) return st;
-    // down: all slots of R output row groups per CTA, about two CTAs per SM
     const int64_t n_rg = (hidden + 3) / 4;
-    const int64_t dn_rgb = 4 * down->cols_pad;
-    // codes of dn_r row groups per slot, plus act (slots x cols_pad floats = one row group's bytes per slot)
-    int64_t dn_r = kFfnSmem / (slots * dn_rgb) - 1;
-    if (dn_r > kDnMaxUnits / slots) dn_r = kDnMaxUnits / slots;
-    if (dn_r >= 1) {
-        const int64_t want = (n_rg + 2 * sms - 1) / (2 * sms);
-        if (dn_r > want) dn_r = want < 1 ? 1 : want;
-        return qmv::launch_pdl(moe_down_smem_kernel, dim3((unsigned)((n_rg + dn_r - 1) / dn_r)), dim3(kThreads),
-                               (size_t)(slots * (dn_r + 1) * dn_rgb), cs, down->q, down->rs, E, hidden, down->rows_pad,
-                               down->cols_pad, (int)dn_r, sel, w, slots, act, astride, out, status);
+    if (plan.dn_r >= 1) {
+        const int64_t dn_rgb = 4 * down->cols_pad;
+        const size_t smem = (size_t)(slots * (plan.dn_r + 1) * dn_rgb);
+        return qmv::launch_pdl(moe_down_smem_kernel,
+                               dim3((unsigned)((n_rg + plan.dn_r - 1) / plan.dn_r)), dim3(kThreads), smem, cs,
+                               down->q, down->rs, E, hidden, down->rows_pad, down->cols_pad, (int)plan.dn_r, sel, w,
+                               slots, act, astride, out, status);
     }
     const int nw = slots < kDownMaxWarps ? slots : kDownMaxWarps;
     return qmv::launch_pdl(moe_down_kernel, dim3((unsigned)((n_rg + kDownR - 1) / kDownR)), dim3(nw * 32), 0, cs,
@@ -935,6 +975,34 @@ extern "C" qmv_status moe_ffn_q8row(const qmv_weights* gate, const qmv_weights* 
     const qmv_status s = launch_ffn(gate, up, down, sel, w, slots, x, out, act, status, cs);
     cudaFreeAsync(act, cs);
     return s;
+}
+
+// ---------------------------------------------------------------------------
+// moe_step_q8row: moe_select_topk + moe_ffn_q8row in one call (the same
+// three kernels).  Making the selection inside the FFN kernels instead was
+// measured slower on this part: the gate/up CTAs fill shared memory, so the
+// down CTAs mostly start after gate/up and could no longer fetch their codes
+// before their dependency wait.
+// ---------------------------------------------------------------------------
+extern "C" qmv_status moe_step_q8row(const float* logits, int n_exp, int top_k, int renorm, const float* sg_w,
+                                     const float* sg_logit, const qmv_weights* gate, const qmv_weights* up,
+                                     const qmv_weights* down, const float* x, int32_t* sel, float* w, float* out,
+                                     qmv_stream st) {
+    QMV_REQUIRE(logits && sel && w, QMV_ERR_INVALID_ARG, "moe_step_q8row: null argument");
+    QMV_REQUIRE(n_exp >= 1 && n_exp <= kSelMaxExperts, QMV_ERR_INVALID_ARG,
+                "moe_step_q8row: need 1 <= n_exp <= %d (got %d)", kSelMaxExperts, n_exp);
+    QMV_REQUIRE(top_k >= 1 && top_k <= n_exp, QMV_ERR_INVALID_ARG,
+                "moe_step_q8row: need 1 <= top_k <= n_exp (got %d)", top_k);
+    const int shared = (sg_w || sg_logit) ? 1 : 0;
+    const int slots = top_k + shared;
+    const qmv_status a = check_ffn_args("moe_step_q8row", gate, up, down, sel, w, slots, x, out);
+    if (a != QMV_OK) return a;
+    QMV_REQUIRE(gate->experts >= n_exp + shared, QMV_ERR_INVALID_ARG,
+                "moe_step_q8row: the expert stacks hold %lld experts, the router needs %d",
+                (long long)gate->experts, n_exp + shared);
+    const qmv_status s1 = moe_select_topk(logits, n_exp, top_k, renorm, sg_w, x, (int)gate->cols, sg_logit, sel, w, st);
+    if (s1 != QMV_OK) return s1;
+    return moe_ffn_q8row(gate, up, down, sel, w, slots, x, out, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -30,14 +30,14 @@
  *    them with qmv_weights_free() after all work that reads them is done.
  *  - Thread safety: calls that read a handle may run concurrently; packing
  *    and freeing a handle need external ordering.
- *  - The decode kernels (qmv_q8row, moe_select_topk, moe_ffn_q8row*) are
- *    programmatic dependent launches: each may start while the previous
- *    kernel in `st` is still running, and before waiting for it reads only
- *    packed weights (and, in the down kernel of the expert FFN, sel and w,
- *    which the FFN's own first kernel has already waited for).  Activations,
- *    selections and outputs are read or written only after that wait, so
- *    stream order holds as usual.  Packed weights must not be written by
- *    the kernel that precedes such a call.
+ *  - The decode kernels (qmv_q8row, qmv_q2g64/g128, moe_select_topk,
+ *    moe_ffn_q8row*, moe_step_q8row) are programmatic dependent launches:
+ *    each may start while the previous kernel in `st` is still running, and
+ *    before waiting for it reads only packed weights -- except the second
+ *    kernel of the expert FFN, which may also read that call's sel and w,
+ *    since the call's first kernel has already waited for them.  Everything
+ *    else is read or written after the wait, so stream order holds as usual.  Packed weights must not be written by the kernel that
+ *    precedes such a call.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -197,6 +197,23 @@ QMV_API qmv_status moe_ffn_q8row(const qmv_weights *gate, const qmv_weights *up,
                          const qmv_weights *down, const int32_t *sel,
                          const float *w, int slots, const float *x,
                          float *out, qmv_stream st);
+
+/* One MoE decode step in one call: moe_select_topk followed by
+ * moe_ffn_q8row, with the same arguments and the same results bit for bit
+ * (the same three kernels).
+ *   logits [n_exp], sg_w [hidden] or sg_logit [1] or neither, as in
+ *   moe_select_topk; x [hidden], out [hidden] as in moe_ffn_q8row with
+ *   hidden = gate's cols; slots = top_k (+1 with a shared expert) <= 64.
+ *   The expert stacks must hold at least n_exp (+1) experts; the shared
+ *   expert is number n_exp.
+ *   Outputs: sel [slots] int32, w [slots] f32 (the selection, as
+ *   moe_select_topk writes it) and out.
+ * Uses a stream-ordered scratch allocation of slots*inter*4 bytes. */
+QMV_API qmv_status moe_step_q8row(const float *logits, int n_exp, int top_k,
+                          int renorm, const float *sg_w, const float *sg_logit,
+                          const qmv_weights *gate, const qmv_weights *up,
+                          const qmv_weights *down, const float *x,
+                          int32_t *sel, float *w, float *out, qmv_stream st);
 
 /* Allocation-free variant of moe_ffn_q8row, for callers that cannot
  * allocate device memory while serving (engines that give all device memory

@@ -137,9 +137,10 @@ def moe_chain(qmv):
     return _pack(qmv, dataclasses.replace(m, drs=(m.drs / rms).astype(np.float32)))
 
 
-def _moe_steps(qmv, moe, sync, static, chain_x):
+def _moe_steps(qmv, moe, sync, static, chain_x, fused=False):
     """STEPS router + FFN steps with shared sel / w (and act scratch), each
-    with its own logits; with chain_x, step i+1 takes step i's output as x."""
+    with its own logits; with chain_x, step i+1 takes step i's output as x;
+    fused: one moe_step_q8row call per step."""
     m, (gate, up, down) = moe
     bank = dev(synth.logit_bank(E, STEPS, 310))
     sgw = dev(m.sgw)
@@ -153,8 +154,12 @@ def _moe_steps(qmv, moe, sync, static, chain_x):
     with torch.cuda.stream(s):
         for i in range(STEPS):
             x = xs[i] if chain_x else xs[0]
-            qmv.moe_select_topk(bank[i], K, True, sg_w=sgw, x=x, sel=sel, w=w, stream=s)
-            ffn(gate, up, down, sel, w, x, xs[i + 1], stream=s)
+            if fused:
+                qmv.moe_step_q8row(bank[i], K, True, gate, up, down, x, sg_w=sgw, sel=sel, w=w, out=xs[i + 1],
+                                   stream=s)
+            else:
+                qmv.moe_select_topk(bank[i], K, True, sg_w=sgw, x=x, sel=sel, w=w, stream=s)
+                ffn(gate, up, down, sel, w, x, xs[i + 1], stream=s)
             if sync:
                 s.synchronize()
                 sels.append(host(sel).copy())
@@ -168,11 +173,13 @@ def test_moe_steps_back_to_back(qmv, moe, moe_chain, chain_x):
     moe = moe_chain if chain_x else moe
     fast, _, _ = _moe_steps(qmv, moe, False, False, chain_x)
     fast_static, _, _ = _moe_steps(qmv, moe, False, True, chain_x)
+    fast_fused, _, _ = _moe_steps(qmv, moe, False, False, chain_x, fused=True)
     slow, sels, ws = _moe_steps(qmv, moe, True, False, chain_x)
     assert all(np.isfinite(t).all() for t in slow)
     for i in range(1, STEPS + 1):
         assert np.array_equal(fast[i], slow[i]), f"step {i - 1} differs from the synchronised run"
         assert np.array_equal(fast_static[i], slow[i]), f"static step {i - 1} differs"
+        assert np.array_equal(fast_fused[i], slow[i]), f"fused step {i - 1} differs"
     m, _ = moe
     bank = synth.logit_bank(E, STEPS, 310)
     for i in (0, STEPS - 1):

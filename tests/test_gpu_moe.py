@@ -111,3 +111,42 @@ def test_moe_bad_expert_sets_device_status(qmv):
     with pytest.raises(qmv.QmvError, match="DEVICE_STATUS"):
         qmv.qmv_check()
     assert qmv.qmv_check() == 0   # cleared
+
+
+# (n_exp, hidden, inter, top_k, shared, renorm): the rank path (n_exp <= 256)
+# and the argmax-rounds path (n_exp > 256), with and without a shared expert,
+# with a given shared-gate logit, with and without renormalisation
+FUSED_CASES = [(128, 2048, 768, 8, "sgw", True), (10, 128, 96, 3, "sgw", False), (300, 256, 64, 6, "logit", True),
+               (64, 512, 128, 4, None, True), (7, 64, 48, 7, "sgw", True)]
+
+
+@pytest.mark.parametrize("n_exp,hidden,inter,k,shared,renorm", FUSED_CASES)
+def test_moe_step_fused_matches_separate_and_oracle(qmv, n_exp, hidden, inter, k, shared, renorm):
+    m = synth.moe_inputs(n_exp, hidden, inter, seed=200 + n_exp + k)
+    gate, up, down = _pack_moe(qmv, m)
+    kw, okw = {}, {}
+    if shared == "sgw":
+        kw = dict(sg_w=dev(m.sgw))
+        okw = dict(sgw=m.sgw, x=m.x)
+    elif shared == "logit":
+        kw = dict(sg_logit=dev(np.array([0.3], np.float32)))
+        okw = dict(sg_logit=0.3)
+    sel_f, w_f, out_f = qmv.moe_step_q8row(dev(m.logits), k, renorm, gate, up, down, dev(m.x), **kw)
+    sel_s, w_s = qmv.moe_select_topk(dev(m.logits), k, renorm, x=dev(m.x) if shared == "sgw" else None, **kw)
+    out_s = qmv.moe_ffn_q8row(gate, up, down, sel_s, w_s, dev(m.x))
+    sel_f, w_f, out_f, sel_s, w_s, out_s = (host(t) for t in (sel_f, w_f, out_f, sel_s, w_s, out_s))
+    assert np.array_equal(sel_f, sel_s) and np.array_equal(w_f, w_s)
+    assert np.array_equal(out_f, out_s)
+    sel_ref, w_ref = oracle.select(m.logits, k, renorm, **okw)
+    assert sel_f.tolist() == sel_ref.tolist()
+    np.testing.assert_allclose(w_f.astype(np.float64), w_ref, rtol=TOL_ROUTER_W, atol=0)
+    out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel_ref, w_ref, m.x, with_parts=True)
+    assert_within(out_f, out_ref, moe_bound(m, sel_ref, w_ref, parts), 1.0, "fused moe step")
+
+
+def test_moe_step_rejects_too_few_experts(qmv):
+    m = synth.moe_inputs(8, 64, 32, seed=97)   # stacks of 9 experts (8 routed + the shared one)
+    gate, up, down = _pack_moe(qmv, m)
+    logits = dev(np.zeros(9, np.float32))      # a router over 9 experts needs 10 with the shared one
+    with pytest.raises(qmv.QmvError, match="INVALID_ARG"):
+        qmv.moe_step_q8row(logits, 2, True, gate, up, down, dev(m.x), sg_w=dev(m.sgw))
