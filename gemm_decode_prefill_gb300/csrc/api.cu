@@ -350,4 +350,39 @@ qmv_status qmv_check(qmv_stream st, int* code) {
     return QMV_OK;
 }
 
+// Host-buffer variants of the decode GEMVs: copy x in, run the GEMV, copy y
+// out, all enqueued on st by one call.
+static qmv_status host_gemv(qmv_status (*gemv)(const qmv_weights*, const float*, float*, qmv_stream),
+                            const char* name, const qmv_weights* w, const float* x_host, float* y_host, float* x_dev,
+                            float* y_dev, qmv_stream st) {
+    QMV_REQUIRE(w && x_host && y_host && x_dev && y_dev, QMV_ERR_INVALID_ARG, "%s: null argument", name);
+    cudaStream_t cs = (cudaStream_t)st;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, (size_t)w->cols * sizeof(float), cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return qmv::fail(QMV_ERR_CUDA, "%s: copy of x failed: %s", name, cudaGetErrorString(e));
+    }
+    const qmv_status s = gemv(w, x_dev, y_dev, st);
+    if (s != QMV_OK) return s;
+    e = cudaMemcpyAsync(y_host, y_dev, (size_t)w->rows * sizeof(float), cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return qmv::fail(QMV_ERR_CUDA, "%s: copy of y failed: %s", name, cudaGetErrorString(e));
+    }
+    return QMV_OK;
+}
+
+qmv_status qmv_q8row_host(const qmv_weights* w, const float* xs_host, float* y_host, float* xs_dev, float* y_dev,
+                          qmv_stream st) {
+    return host_gemv(qmv_q8row, "qmv_q8row_host", w, xs_host, y_host, xs_dev, y_dev, st);
+}
+qmv_status qmv_q2g64_host(const qmv_weights* w, const float* x_host, float* y_host, float* x_dev, float* y_dev,
+                          qmv_stream st) {
+    return host_gemv(qmv_q2g64, "qmv_q2g64_host", w, x_host, y_host, x_dev, y_dev, st);
+}
+qmv_status qmv_q2g128_host(const qmv_weights* w, const float* x_host, float* y_host, float* x_dev, float* y_dev,
+                           qmv_stream st) {
+    return host_gemv(qmv_q2g128, "qmv_q2g128_host", w, x_host, y_host, x_dev, y_dev, st);
+}
+
 }  // extern "C"

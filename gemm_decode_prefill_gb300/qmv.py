@@ -42,6 +42,9 @@ _SIGS = {
     "qmv_q2g64": ([_P, _P, _P, _P], _I),
     "qmv_q2g128": ([_P, _P, _P, _P], _I),
     "qmm_q8row": ([_P, _P, _I64, _P, _P], _I),
+    "qmv_q8row_host": ([_P, _P, _P, _P, _P, _P], _I),
+    "qmv_q2g64_host": ([_P, _P, _P, _P, _P, _P], _I),
+    "qmv_q2g128_host": ([_P, _P, _P, _P, _P, _P], _I),
     "moe_select_topk": ([_P, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P], _I),
     "moe_ffn_q8row": ([_P, _P, _P, _P, _P, _I, _P, _P, _P], _I),
     "moe_ffn_q8row_static": ([_P, _P, _P, _P, _P, _I, _P, _P, _P], _I),
@@ -193,6 +196,35 @@ def qmv_q2g64(w: Weights, x: torch.Tensor, y: torch.Tensor | None = None, stream
 
 def qmv_q2g128(w: Weights, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     return _q2(_lib.qmv_q2g128, "qmv_q2g128", w, x, y, stream)
+
+
+def _host_f32(t: torch.Tensor, name: str, n: int) -> int:
+    if t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous() or t.numel() != n:
+        raise ValueError(f"{name}: need a contiguous float32 host tensor of {n} elements")
+    return t.data_ptr()
+
+
+def _gemv_host(fn, name, w: Weights, x_host: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
+               y_dev: torch.Tensor, stream=None):
+    _check(fn(w.handle, _host_f32(x_host, "x_host", w.cols), _host_f32(y_host, "y_host", w.rows),
+              _dev(x_dev, torch.float32, "x_dev", (w.cols,)), _dev(y_dev, torch.float32, "y_dev", (w.rows,)),
+              _stream(stream)), name)
+    return y_host
+
+
+def qmv_q8row_host(w, xs_host, y_host, xs_dev, y_dev, stream=None):
+    """xs (pinned host) -> device, q8_row GEMV, y -> pinned host; one C call."""
+    return _gemv_host(_lib.qmv_q8row_host, "qmv_q8row_host", w, xs_host, y_host, xs_dev, y_dev, stream)
+
+
+def qmv_q2g64_host(w, x_host, y_host, x_dev, y_dev, stream=None):
+    """x (pinned host) -> device, Q2 g64 GEMV, y -> pinned host; one C call."""
+    return _gemv_host(_lib.qmv_q2g64_host, "qmv_q2g64_host", w, x_host, y_host, x_dev, y_dev, stream)
+
+
+def qmv_q2g128_host(w, x_host, y_host, x_dev, y_dev, stream=None):
+    """x (pinned host) -> device, Q2 g128 GEMV, y -> pinned host; one C call."""
+    return _gemv_host(_lib.qmv_q2g128_host, "qmv_q2g128_host", w, x_host, y_host, x_dev, y_dev, stream)
 
 
 def qmm_q8row(w: Weights, xs: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -146,6 +146,22 @@ QMV_API qmv_status qmv_q2g64(const qmv_weights *w, const float *x, float *y,
 QMV_API qmv_status qmv_q2g128(const qmv_weights *w, const float *x, float *y,
                       qmv_stream st);
 
+/* The decode GEMVs with host buffers: one call enqueues on `st` the copy of
+ * x_host [cols] (host) to x_dev [cols] (device), the GEMV into y_dev [rows]
+ * (device) and the copy of y_dev to y_host [rows] (host).  Same results and
+ * argument rules as the device-buffer calls.  Host buffers should be pinned
+ * (page-locked); with pageable memory the copies are staged by the driver
+ * and may synchronize.  y_host is complete when `st` reaches that point. */
+QMV_API qmv_status qmv_q8row_host(const qmv_weights *w, const float *xs_host,
+                          float *y_host, float *xs_dev, float *y_dev,
+                          qmv_stream st);
+QMV_API qmv_status qmv_q2g64_host(const qmv_weights *w, const float *x_host,
+                          float *y_host, float *x_dev, float *y_dev,
+                          qmv_stream st);
+QMV_API qmv_status qmv_q2g128_host(const qmv_weights *w, const float *x_host,
+                           float *y_host, float *x_dev, float *y_dev,
+                           qmv_stream st);
+
 /* ---------------------------------------------------------------------- */
 /* Prefill GEMM                                                           */
 /* ---------------------------------------------------------------------- */

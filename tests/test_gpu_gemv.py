@@ -199,3 +199,33 @@ def test_q2_repeated_calls_are_identical(qmv, group):
     for y in ys:
         assert_within(y, y_ref, mag, TOL_GEMV, f"q2 g{group} repeated")
     assert all(np.array_equal(ys[0], y) for y in ys[1:])
+
+
+@pytest.mark.parametrize("kind", ["q8", "q2g64", "q2g128"])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_calls_match_device_calls(qmv, kind, pinned):
+    """qmv_*_host: copy in, GEMV, copy out in one call; bit-identical to the
+    device-buffer call, from pinned and from pageable host memory."""
+    rows, cols = 1000, 5120
+    if kind == "q8":
+        q, rs, x = synth.q8_inputs(rows, cols, seed=61)
+        w = qmv.qmv_pack_q8row(dev(q), dev(rs))
+        fn, fn_host = qmv.qmv_q8row, qmv.qmv_q8row_host
+    else:
+        group = 64 if kind == "q2g64" else 128
+        codes, d, x = synth.q2_inputs(rows, cols, group, seed=62)
+        w = qmv.qmv_pack_q2(dev(codes), d16(d), group)
+        fn = qmv.qmv_q2g64 if group == 64 else qmv.qmv_q2g128
+        fn_host = qmv.qmv_q2g64_host if group == 64 else qmv.qmv_q2g128_host
+    y_ref = host(fn(w, dev(x)))
+    x_host = torch.from_numpy(x.copy())
+    y_host = torch.full((rows,), float("nan"))
+    if pinned:
+        x_host, y_host = x_host.pin_memory(), y_host.pin_memory()
+    x_dev = torch.empty(cols, device="cuda")
+    y_dev = torch.empty(rows, device="cuda")
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        fn_host(w, x_host, y_host, x_dev, y_dev, stream=s)
+        s.synchronize()
+        assert np.array_equal(y_host.numpy(), y_ref)
