@@ -150,3 +150,24 @@ def test_moe_step_rejects_too_few_experts(qmv):
     logits = dev(np.zeros(9, np.float32))      # a router over 9 experts needs 10 with the shared one
     with pytest.raises(qmv.QmvError, match="INVALID_ARG"):
         qmv.moe_step_q8row(logits, 2, True, gate, up, down, dev(m.x), sg_w=dev(m.sgw))
+
+
+# Shapes too wide for the staged FFN kernels, one per register-streaming
+# fallback: the down projection of 9 slots x 2560 columns (2 x 9 x 10 KB of
+# codes per CTA is over the 96 KB budget); gate/up rows of 12800 columns (x
+# does not fit the 48 KB activation staging); gate/up rows of 9216 columns
+# (x fits, but not three row groups of both matrices).
+FALLBACK_CASES = [(8, 2048, 2560, 8), (2, 12800, 64, 1), (2, 9216, 64, 1)]
+
+
+@pytest.mark.parametrize("n_exp,hidden,inter,k", FALLBACK_CASES)
+def test_moe_step_register_fallbacks(qmv, n_exp, hidden, inter, k):
+    m = synth.moe_inputs(n_exp, hidden, inter, seed=300 + n_exp + hidden)
+    gate, up, down = _pack_moe(qmv, m)
+    sel, w, out = qmv.moe_step_q8row(dev(m.logits), k, True, gate, up, down, dev(m.x), sg_w=dev(m.sgw))
+    sel, w, out = host(sel), host(w), host(out)
+    sel_ref, w_ref = oracle.select(m.logits, k, True, sgw=m.sgw, x=m.x)
+    assert sel.tolist() == sel_ref.tolist()
+    np.testing.assert_allclose(w.astype(np.float64), w_ref, rtol=TOL_ROUTER_W, atol=0)
+    out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel_ref, w_ref, m.x, with_parts=True)
+    assert_within(out, out_ref, moe_bound(m, sel_ref, w_ref, parts), 1.0, f"moe fallback {hidden}x{inter}")
