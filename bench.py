@@ -625,6 +625,13 @@ def run_rows_only(launches: int = 0):
     for i in range(launches):
         qmv.moe_step_q8row(bank[i % 64], cfg["top_k"], cfg["renorm"], gate, upw, down, xm, sg_w=sgw, sel=sel,
                            w=wsel, out=out, stream=stream)
+    cfg = synth.WORKLOADS["q8_prefill_gemm_17408x5120_nb512"]
+    q, rs, xs = synth.qmm_inputs(cfg["rows"], cfg["cols"], cfg["nb"], cfg["seed"])
+    wg = qmv.qmv_pack_q8row(up(q), up(rs), stream=stream)
+    xg = up(xs)
+    yg = torch.empty(cfg["nb"], cfg["rows"], device=dev)
+    for i in range(launches):
+        qmv.qmm_q8row(wg, xg, yg, stream=stream)
     torch.cuda.synchronize()
     return {"rows": "untimed", "launches": launches, "impl": "ours"}
 
@@ -640,8 +647,8 @@ def main(argv=None):
     ap.add_argument("--rows-only", action="store_true",
                     help="only the other workloads (q8 GEMVs, prefill GEMM, MoE step), one JSON line; for profiling")
     ap.add_argument("--launches", type=int, default=0,
-                    help="with --rows-only: just N untimed eager calls of the q8 4096x4096 GEMV and the MoE step "
-                         "(a small program for ncu captures)")
+                    help="with --rows-only: just N untimed eager calls of the q8 4096x4096 GEMV, the MoE step and "
+                         "the prefill GEMM (a small program for ncu captures)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     args = ap.parse_args(argv)

@@ -228,8 +228,14 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- dequant: int8 -> bf16, swizzled K-major ----------------
-        const int t = threadIdx.x - 128;    // 0..127
-        const int rg = t >> 2, qd = t & 3;  // row group, 16-column quarter
+        // The int8 tile is [32 row groups][16 lanes][16 bytes = 4 rows x 4
+        // columns].  Dequant warp wd reads row groups 8wd..8wd+7 as four
+        // 512-byte runs (one 16-byte chunk per thread, conflict-free); thread
+        // lane then holds columns 4(lane%16)..+3 of the 4 rows of row groups
+        // 8wd + 2j + lane/16, j = 0..3, and writes each row's 4 bf16 as one
+        // 8-byte store into the 128-byte-swizzled tile.
+        const int wd = warp - 4;            // 0..3
+        const int l16 = lane & 15, hh = lane >> 4;
         int it = 0;
         for (int tile = blockIdx.x; tile < num_tiles && !*abort; tile += gridDim.x) {
             bool ok = true;
@@ -237,22 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_
                 const int s = it % STAGES;
                 const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
                 if (!mbar_wait(&sm.full[s], ph, abort, status)) { ok = false; break; }
-                const uint4* src = reinterpret_cast<const uint4*>(sm.a8[s] + rg * 256 + qd * 64);
-                const uint4 c0 = src[0], c1 = src[1], c2 = src[2], c3 = src[3];
-                const uint32_t w[4][4] = {{c0.x, c1.x, c2.x, c3.x},
-                                          {c0.y, c1.y, c2.y, c3.y},
-                                          {c0.z, c1.z, c2.z, c3.z},
-                                          {c0.w, c1.w, c2.w, c3.w}};
+                const uint4* src = reinterpret_cast<const uint4*>(sm.a8[s]) + wd * 128 + lane;
+                uint4 c[4];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    const int m = rg * 4 + rr;
-                    uint32_t o[8];
+                for (int j = 0; j < 4; ++j) c[j] = src[j * 32];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) i8x4_to_bf16(w[rr][i], o[2 * i], o[2 * i + 1]);
-                    uint8_t* rowp = sm.a[s] + (m >> 3) * 1024 + (m & 7) * 128;
-                    const int ch0 = (2 * qd) ^ (m & 7), ch1 = (2 * qd + 1) ^ (m & 7);
-                    *reinterpret_cast<uint4*>(rowp + ch0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-                    *reinterpret_cast<uint4*>(rowp + ch1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
+                for (int j = 0; j < 4; ++j) {
+                    const int rg = 8 * wd + 2 * j + hh;
+                    const uint32_t wv[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const int m = rg * 4 + rr;
+                        uint32_t lo, hi;
+                        i8x4_to_bf16(wv[rr], lo, hi);
+                        uint8_t* rowp = sm.a[s] + (m >> 3) * 1024 + (m & 7) * 128;
+                        const int ch = (l16 >> 1) ^ (m & 7);
+                        *reinterpret_cast<uint2*>(rowp + ch * 16 + (l16 & 1) * 8) = make_uint2(lo, hi);
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
