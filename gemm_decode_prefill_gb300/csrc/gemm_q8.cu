@@ -46,6 +46,7 @@ struct __align__(1024) Smem {
     uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t mma_done;   // every MMA this CTA issued has completed
     uint32_t tmem_base;
     int abort;
 };
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_
             mbar_init(&sm.tfull[a], 1);
             mbar_init(&sm.tempty[a], 4);
         }
+        mbar_init(&sm.mma_done, 1);
         sm.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -193,10 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_
                     tma_load_2d(sm.b[s], &tmB, &sm.full[s], ks * BK, nt * BN);
                 }
             }
-            // Drain: every issued copy must land before the CTA can exit.
+            // Drain: every issued copy must land before the CTA can exit, also
+            // after an abort.
             for (int k = 0; k < STAGES && it - 1 - k >= 0; ++k) {
                 const int j = it - 1 - k;
-                mbar_wait(&sm.full[j % STAGES], (uint32_t)(j / STAGES) & 1u, abort, status);
+                qmv::mbar_drain(&sm.full[j % STAGES], (uint32_t)(j / STAGES) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -225,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1) qmm_q8row_tc_kernel(const __grid_
                 if (!ok) break;
                 umma_commit(&sm.tfull[acc]);
             }
+            // every issued MMA must complete before the tensor memory is
+            // released, also after an abort
+            umma_commit(&sm.mma_done);
+            qmv::mbar_drain(&sm.mma_done, 0u);
         }
     } else if (warp >= 4 && warp < 8) {
         // ---------------- dequant: int8 -> bf16, swizzled K-major ----------------

@@ -685,8 +685,7 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
             // drain the last round's copies before the CTA may exit
             if (issued_rounds > 0) {
                 const int64_t r = issued_rounds - 1;
-                for (int i = 0; i < TR && t0 + r * TR + i < t1; ++i)
-                    qmv::mbar_wait(&tfull[i], (uint32_t)r & 1u, abort, status);
+                for (int i = 0; i < TR && t0 + r * TR + i < t1; ++i) qmv::mbar_drain(&tfull[i], (uint32_t)r & 1u);
             }
         }
         return;
