@@ -191,3 +191,41 @@ def test_moe_steps_back_to_back(qmv, moe, moe_chain, chain_x):
         out_ref, parts = oracle.moe_ffn(m.gq, m.grs, m.uq, m.urs, m.dq, m.drs, sel_ref, w_ref, mi.x,
                                         with_parts=True)
         assert_within(slow[i + 1], out_ref, moe_bound(mi, sel_ref, w_ref, parts), 1.0, f"moe step {i}")
+
+
+def test_mixed_chain_q8_then_q2(qmv):
+    """q8 [5120 x 2048] -> Q2 g64 [2048 x 5120] -> Q2 g128 [5120 x 2048]: each
+    stage reads the previous stage's output; the Q2 widths use the persistent
+    kernel."""
+    from gpu_helpers import d16
+    q, rs, _ = synth.q8_inputs(5120, 2048, 320)
+    wa = qmv.qmv_pack_q8row(dev(q), dev(rs))
+    c64, d64, _ = synth.q2_inputs(2048, 5120, 64, 321)
+    wb = qmv.qmv_pack_q2(dev(c64), d16(d64), 64)
+    c128, d128, _ = synth.q2_inputs(5120, 2048, 128, 322)
+    wc = qmv.qmv_pack_q2(dev(c128), d16(d128), 128)
+    x0 = synth.rng(323).standard_normal(2048).astype(np.float32)
+    torch.cuda.synchronize()
+
+    def run(sync):
+        s = torch.cuda.Stream()
+        bufs = [dev(x0), torch.full((5120,), float("nan"), device="cuda"),
+                torch.full((2048,), float("nan"), device="cuda"), torch.full((5120,), float("nan"), device="cuda")]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for k, (fn, w) in enumerate(((qmv.qmv_q8row, wa), (qmv.qmv_q2g64, wb), (qmv.qmv_q2g128, wc))):
+                fn(w, bufs[k], bufs[k + 1], stream=s)
+                if sync:
+                    s.synchronize()
+        torch.cuda.synchronize()
+        return [host(b) for b in bufs]
+
+    fast, slow = run(False), run(True)
+    for i in range(1, 4):
+        assert np.array_equal(fast[i], slow[i]), f"stage {i} differs from the synchronised run"
+    y_ref, mag = oracle.q8row(q, rs, fast[0], with_mag=True)
+    assert_within(fast[1], y_ref, mag, TOL_GEMV, "mixed chain q8")
+    y_ref, mag = oracle.q2(c64, d64, 64, fast[1], with_mag=True)
+    assert_within(fast[2], y_ref, mag, TOL_GEMV, "mixed chain q2 g64")
+    y_ref, mag = oracle.q2(c128, d128, 128, fast[2], with_mag=True)
+    assert_within(fast[3], y_ref, mag, TOL_GEMV, "mixed chain q2 g128")
