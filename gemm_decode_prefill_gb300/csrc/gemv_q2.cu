@@ -14,6 +14,11 @@
 //     (x = hi + mid + lo, 24 significant bits) that form B columns 0..2, so
 //     (q-1)*x is formed without rounding and summed in fp32;
 //   * the per-group scale d (f16 -> f32, exact) multiplies the fp32 group sum.
+// The persistent kernel (q2_gemv_v3_kernel) halves the decode again: one AND
+// per pair of weights leaves q * 2^(p-133) as an exact bf16 subnormal, x
+// enters as three base-256 digits on a common grid so that every group sum
+// the tensor core forms is exact, and the bias -sum(x) of each group is added
+// in fp32 from the digit sums (exact where all weights of a group are 0).
 // The K range is split across the warps of a CTA; partial sums are reduced
 // in shared memory in a fixed order (deterministic).  The persistent kernel
 // is a programmatic dependent launch: its producer warp starts fetching the
@@ -180,14 +185,40 @@ __device__ __forceinline__ void q2_pair_chunk(const uint4 wa, const uint4 wb, co
     }
 }
 
+// Decode for the persistent kernel: the code bits are moved into the low
+// mantissa bits of a zero-exponent bf16, which is the subnormal (or, for
+// bit 7, the smallest normal) number q * 2^(p-133) -- exactly, because
+// bf16 values below 2^-125 are evenly spaced at 2^-133.  One AND per pair
+// of weights and one shift per word, no bias FMA; the bias (q - 1) is
+// applied per group in fp32 (see q2_gemv_v3_kernel).  Register t takes the
+// codes at bits 2t and 2t+16 as before, so p = 0, 2, 4, 6 for the four
+// A registers of a k-step: row r gets p = 0 (columns 0-7 of the step) and
+// 4 (columns 8-15), row r+8 gets 2 and 6.  The activation for columns 8-15
+// is pre-scaled by 2^-4, so every product carries the same factor, times
+// 4 on rows r+8.
+__device__ __forceinline__ void q2_decode_word_sub(uint32_t w, uint32_t a[8]) {
+    const uint32_t w8 = w >> 8;
+    a[0] = w & 0x00030003u;
+    a[1] = w & 0x000C000Cu;
+    a[2] = w & 0x00300030u;
+    a[3] = w & 0x00C000C0u;
+    a[4] = w8 & 0x00030003u;
+    a[5] = w8 & 0x000C000Cu;
+    a[6] = w8 & 0x00300030u;
+    a[7] = w8 & 0x00C000C0u;
+}
+
 // One 16-row tile x 128-column chunk from shared memory: 8 MMA k-steps with
 // zero-initialised group accumulators, d applied per group in fp32.
 // bq: the lane's activation fragments for the chunk ({step 2i, 2i+1} in
 // bq[i]); s01/s23: the lane's raw f16 scales (G=64: (row r: g0, g1) and
-// (row r+8: g0, g1); G=128: s01 = (row r, row r+8)).
+// (row r+8: g0, g1); G=128: s01 = (row r, row r+8)); kk: the lane's bias
+// terms of the chunk's groups (G=64: g0, g1; G=128: .x).  The MMA sums are
+// exact (see q2_gemv_v3_kernel), so adding kk to the rounded column-pair
+// sum cancels exactly where the weights are all zero.
 template <int G>
 __device__ __forceinline__ void q2_tile_chunk_v3(const uint4 w, const uint4 bq[4], uint32_t s01, uint32_t s23,
-                                                 float acc[2]) {
+                                                 float2 kk, float acc[2]) {
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&s01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&s23));
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -195,18 +226,19 @@ __device__ __forceinline__ void q2_tile_chunk_v3(const uint4 w, const uint4 bq[4
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t a[8];
-        q2_decode_word(ws[j], a);
+        q2_decode_word_sub(ws[j], a);
         const bool first = (G == 64) ? ((j & 1) == 0) : (j == 0);
         if (first) mma_bf16_z(c, a[0], a[1], a[2], a[3], bq[j].x, bq[j].y);
         else mma_bf16_acc(c, a[0], a[1], a[2], a[3], bq[j].x, bq[j].y);
         mma_bf16_acc(c, a[4], a[5], a[6], a[7], bq[j].z, bq[j].w);
         if (G == 64 && (j & 1)) {
             const bool g1 = j == 3;
-            acc[0] = fmaf(g1 ? f01.y : f01.x, c[0] + c[1], acc[0]);
-            acc[1] = fmaf(g1 ? f23.y : f23.x, c[2] + c[3], acc[1]);
+            const float k = g1 ? kk.y : kk.x;
+            acc[0] = fmaf(g1 ? f01.y : f01.x, (c[0] + c[1]) + k, acc[0]);
+            acc[1] = fmaf(g1 ? f23.y : f23.x, fmaf(4.f, k, c[2] + c[3]), acc[1]);
         } else if (G == 128 && j == 3) {
-            acc[0] = fmaf(f01.x, c[0] + c[1], acc[0]);
-            acc[1] = fmaf(f01.y, c[2] + c[3], acc[1]);
+            acc[0] = fmaf(f01.x, (c[0] + c[1]) + kk.x, acc[0]);
+            acc[1] = fmaf(f01.y, fmaf(4.f, kk.x, c[2] + c[3]), acc[1]);
         }
     }
 }
@@ -613,8 +645,8 @@ Q2PlanV3 q2_plan_v3(int KC) {
     Q2PlanV3 p{};
     p.code_bytes = (uint32_t)KC * 512;
     p.tile_bytes = p.code_bytes + (uint32_t)KC * 32 * gpc;
-    const size_t fixed = (size_t)KC * 52 * sizeof(uint4) + kV3Warps * 32 * sizeof(float) +
-                         (2 * kV3MaxTR + 2) * sizeof(uint64_t) + 16 + 128;
+    const size_t fixed = (size_t)KC * 52 * sizeof(uint4) + (size_t)KC * 4 * sizeof(float2) +
+                         kV3Warps * 32 * sizeof(float) + (2 * kV3MaxTR + 2) * sizeof(uint64_t) + 16 + 128;
     p.ok = false;
     if (KC > kTmaMaxChunks) return p;   // the activation prologue covers at most kTmaMaxChunks chunks
     for (int tr = kV3MaxTR; tr >= 1; tr >>= 1) {
@@ -638,7 +670,8 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
     uint4* bfrag = reinterpret_cast<uint4*>(base + (size_t)TR * tile_bytes);
-    float* red = reinterpret_cast<float*>(bfrag + (size_t)KC * 52);       // [16 warps][32]
+    float2* ktab = reinterpret_cast<float2*>(bfrag + (size_t)KC * 52);   // [KC][lane % 4] bias terms
+    float* red = reinterpret_cast<float*>(ktab + (size_t)KC * 4);         // [16 warps][32]
     uint64_t* tfull = reinterpret_cast<uint64_t*>(red + kV3Warps * 32);   // [TR]
     uint64_t* cdone = tfull + kV3MaxTR;                                   // [TR]
     uint64_t* rdone = cdone + kV3MaxTR;                                   // round finished
@@ -695,14 +728,32 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
     qmv::pdl_wait();
     qmv::pdl_launch_dependents();
 
-    // ---------------- activation split into B fragments ----------------
-    // Layout per chunk: [k-step pair j][13 slots] uint4; slot l (< 12) holds
-    // lane l's registers for k-steps 2j and 2j+1, slot 12 is zero, so the
-    // four 128-bit loads of a chunk are conflict-free (consecutive lanes,
-    // consecutive 16-byte slots; lanes 12..31 broadcast the zero slot).
-    // Every thread issues all of its activation loads before using any.
+    // ---------------- activation digits into B fragments ----------------
+    // x is written as three base-256 digits on one grid set by the largest
+    // |x| (exponent emax): x ~= 2^(emax-7) * (n0 + n1/256 + n2/65536) with
+    // integers |n0| <= 256, |n1|, |n2| <= 128, an error of at most
+    // 2^(emax-24) per element.  B column p holds digit n_p as the bf16
+    // n_p * 2^(118-8p) for columns 0-7 of a k-step and n_p * 2^(114-8p) for
+    // columns 8-15.  Against the decoded weights q * 2^(p'-133), every
+    // product in column p is then an integer multiple of 2^(-15-8p) (of
+    // 2^(-13-8p) on rows r+8) and a group's sum stays below 2^17 of those
+    // units, so the MMA sums are exact whatever order the tensor core adds
+    // in.  The bias -sum_{k in g} x_k enters through ktab: -N_p * 2^(-15-8p)
+    // with N_p the group's (exact) digit sum, added once per group to the
+    // column-pair sum of lane class 0 (columns 0 and 1, rounded once, as the
+    // pair sum is) and of lane class 1 (column 2).  The loop therefore
+    // leaves rows r scaled by 2^(-8-emax) and rows r+8 by 2^(-6-emax).
+    //
+    // Fragment layout per chunk: [k-step pair j][13 slots] uint4; slot l
+    // (< 12) holds lane l's registers for k-steps 2j and 2j+1, slot 12 is
+    // zero, so the four 128-bit loads of a chunk are conflict-free
+    // (consecutive lanes, consecutive 16-byte slots; lanes 12..31 broadcast
+    // the zero slot).  Every thread issues all of its activation loads before
+    // using any.
+    int emax;
     {
         constexpr int kMaxPer = (kTmaMaxChunks * 32 + kV3Warps * 32 - 1) / (kV3Warps * 32);
+        constexpr int kItemsPerGroup = G / 4;   // 4 threads per 16-column k-step
         const int n = KC * 32;
         float2 lo[kMaxPer], hi[kMaxPer];
 #pragma unroll
@@ -717,21 +768,63 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
                 }
             }
         }
+        float m = 0.f;
+#pragma unroll
+        for (int u = 0; u < kMaxPer; ++u)
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(lo[u].x), fabsf(lo[u].y)), fmaxf(fabsf(hi[u].x), fabsf(hi[u].y))));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[warp] = m;
+        qmv::named_bar(1, kV3Warps * 32);
+        float mx = 0.f;
+#pragma unroll
+        for (int w = 0; w < kV3Warps; ++w) mx = fmaxf(mx, red[w]);
+        // clamped so that 2^(7-emax) and every scale below is a normal float
+        emax = min(max((int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -120), 127);
+        const float sc = __uint_as_float((uint32_t)(134 - emax) << 23);   // 2^(7-emax)
+        const float kLo[3] = {0x1p118f, 0x1p110f, 0x1p102f};
+        const float kHi[3] = {0x1p114f, 0x1p106f, 0x1p98f};
 #pragma unroll
         for (int u = 0; u < kMaxPer; ++u) {
             const int e = threadIdx.x + u * kV3Warps * 32;
-            if (e < n) {
+            if (e < n) {   // n is a multiple of 32: uniform across the warp
                 const int s = e >> 2, kq = e & 3;
                 const float xv[4] = {lo[u].x, lo[u].y, hi[u].x, hi[u].y};
-                __nv_bfloat16 p[3][4];
+                float dg[3][4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) split3(xv[q], p[0][q], p[1][q], p[2][q]);
+                for (int q = 0; q < 4; ++q) {
+                    const float t = xv[q] * sc;
+                    dg[0][q] = rintf(t);
+                    const float r1 = (t - dg[0][q]) * 256.f;
+                    dg[1][q] = rintf(r1);
+                    dg[2][q] = rintf((r1 - dg[1][q]) * 256.f);
+                }
                 uint2* chunk = reinterpret_cast<uint2*>(bfrag + (size_t)(s >> 3) * 52);
                 const int j = (s & 7) >> 1, half = s & 1;
 #pragma unroll
-                for (int part = 0; part < 3; ++part)
-                    chunk[(j * 13 + part * 4 + kq) * 2 + half] =
-                        make_uint2(pack_bf16x2(p[part][0], p[part][1]), pack_bf16x2(p[part][2], p[part][3]));
+                for (int p = 0; p < 3; ++p) {
+                    const __nv_bfloat162 b0 = __floats2bfloat162_rn(dg[p][0] * kLo[p], dg[p][1] * kLo[p]);
+                    const __nv_bfloat162 b1 = __floats2bfloat162_rn(dg[p][2] * kHi[p], dg[p][3] * kHi[p]);
+                    chunk[(j * 13 + p * 4 + kq) * 2 + half] =
+                        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+                }
+                // the group's digit sums (integers below 2^15: exact)
+                float ns[3];
+#pragma unroll
+                for (int p = 0; p < 3; ++p) ns[p] = (dg[p][0] + dg[p][1]) + (dg[p][2] + dg[p][3]);
+#pragma unroll
+                for (int o = 1; o < kItemsPerGroup; o <<= 1)
+#pragma unroll
+                    for (int p = 0; p < 3; ++p) ns[p] += __shfl_xor_sync(0xffffffffu, ns[p], o);
+                const int gl = e & (kItemsPerGroup - 1);
+                if (gl < 4) {   // item gl writes the bias of lane class gl
+                    const float b01 = -ns[0] * 0x1p-15f + -ns[1] * 0x1p-23f;
+                    const float kv = gl == 0 ? b01 : (gl == 1 ? -ns[2] * 0x1p-31f : 0.f);
+                    const int grp = e / kItemsPerGroup;
+                    float* kt = reinterpret_cast<float*>(ktab + (size_t)(grp / gpc) * 4 + gl);
+                    kt[grp % gpc] = kv;
+                    if (gpc == 1) kt[1] = 0.f;
+                }
             }
         }
         for (int c = threadIdx.x; c < KC * 4; c += kV3Warps * 32)
@@ -751,11 +844,12 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
             const uint8_t* ts = base + (size_t)ti * tile_bytes + code_bytes;
             float acc[2] = {0.f, 0.f};
             float acc2[2] = {0.f, 0.f};
-            auto chunk_args = [&](int c, uint4 (&bq)[4], uint4& w, uint32_t& s01, uint32_t& s23) {
+            auto chunk_args = [&](int c, uint4 (&bq)[4], uint4& w, uint32_t& s01, uint32_t& s23, float2& kk) {
                 const uint4* bsrc = bfrag + (size_t)c * 52 + bl;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) bq[j] = bsrc[j * 13];
                 w = tc[(size_t)c * 32 + lane];
+                kk = ktab[(size_t)c * 4 + (lane & 3)];
                 if (G == 64) {
                     const uint2 v = reinterpret_cast<const uint2*>(ts + (size_t)c * 64)[lane >> 2];
                     s01 = v.x;
@@ -769,16 +863,18 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
             for (; c + 1 < cz; c += 2) {   // two chunks per step: two independent MMA chains
                 uint4 bq0[4], bq1[4], w0, w1;
                 uint32_t s0a, s0b, s1a, s1b;
-                chunk_args(c, bq0, w0, s0a, s0b);
-                chunk_args(c + 1, bq1, w1, s1a, s1b);
-                q2_tile_chunk_v3<G>(w0, bq0, s0a, s0b, acc);
-                q2_tile_chunk_v3<G>(w1, bq1, s1a, s1b, acc2);
+                float2 k0, k1;
+                chunk_args(c, bq0, w0, s0a, s0b, k0);
+                chunk_args(c + 1, bq1, w1, s1a, s1b, k1);
+                q2_tile_chunk_v3<G>(w0, bq0, s0a, s0b, k0, acc);
+                q2_tile_chunk_v3<G>(w1, bq1, s1a, s1b, k1, acc2);
             }
             if (c < cz) {
                 uint4 bq0[4], w0;
                 uint32_t s0a, s0b;
-                chunk_args(c, bq0, w0, s0a, s0b);
-                q2_tile_chunk_v3<G>(w0, bq0, s0a, s0b, acc);
+                float2 k0;
+                chunk_args(c, bq0, w0, s0a, s0b, k0);
+                q2_tile_chunk_v3<G>(w0, bq0, s0a, s0b, k0, acc);
             }
             acc[0] += acc2[0];
             acc[1] += acc2[1];
@@ -799,7 +895,8 @@ __global__ void __launch_bounds__(kV3Threads, 1) q2_gemv_v3_kernel(
                     float sum = 0.f;
                     for (int k = 0; k < WPT; ++k) sum += red[(warp + k) * 32 + lane];
                     const int64_t row = t * 16 + lane;
-                    if (row < rows) y[row] = sum;
+                    // undo the digit grid and the 4x of rows r+8 (exact)
+                    if (row < rows) y[row] = ldexpf(sum, (lane < 8 ? 8 : 6) + emax);
                 }
                 __syncwarp();
             }

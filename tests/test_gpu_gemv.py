@@ -172,9 +172,10 @@ def test_q2_all_zero_weights_give_exact_zero(qmv, group):
 
 @pytest.mark.parametrize("scale", [1e-30, 1e-6, 1.0, 1e6, 1e30])
 def test_q2_activation_magnitudes(qmv, scale):
-    """The split of x into e4m3 parts follows max|x|: results stay inside the
-    bound across 60 decades of activation size and with a wide dynamic range
-    inside one vector."""
+    """The activation parts follow max|x| (exact bf16 parts in the tiled
+    kernels, base-256 digits on a grid set by max|x| in the persistent one):
+    results stay inside the bound across 60 decades of activation size and
+    with a wide dynamic range inside one vector."""
     rows, cols = 520, 1024
     codes, d, x = synth.q2_inputs(rows, cols, 64, seed=59)
     x = (x * scale).astype(np.float32)
