@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "qmv_internal.cuh"
 
@@ -308,6 +310,80 @@ qmv_status qmv_pack_q2(const uint8_t* codes, const uint16_t* d, int group, int64
         return s;
     }
     *out = w;
+    return QMV_OK;
+}
+
+qmv_status qmv_q2_blocks_to_planar(const void* blocks, int group, int64_t rows, int64_t cols, uint8_t* codes,
+                                   uint16_t* d) {
+    QMV_REQUIRE(blocks && codes && d, QMV_ERR_INVALID_ARG, "qmv_q2_blocks_to_planar: null argument");
+    QMV_REQUIRE(group == 64 || group == 128, QMV_ERR_INVALID_ARG,
+                "qmv_q2_blocks_to_planar: group must be 64 or 128 (got %d)", group);
+    QMV_REQUIRE(rows >= 1 && cols >= group && cols % group == 0, QMV_ERR_INVALID_ARG,
+                "qmv_q2_blocks_to_planar: need rows >= 1 and cols a positive multiple of the group "
+                "(rows=%lld cols=%lld)", (long long)rows, (long long)cols);
+    const int64_t nb = cols / group, qbytes = group / 4, bs = 2 + qbytes;
+    const uint8_t* src = static_cast<const uint8_t*>(blocks);
+    for (int64_t m = 0; m < rows; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const uint8_t* blk = src + (m * nb + b) * bs;
+            d[m * nb + b] = (uint16_t)((unsigned)blk[0] | ((unsigned)blk[1] << 8));   // little-endian f16
+            memcpy(codes + m * (cols / 4) + b * qbytes, blk + 2, (size_t)qbytes);
+        }
+    }
+    return QMV_OK;
+}
+
+qmv_status qmv_pack_q2_blocks(const void* blocks, int group, int64_t rows, int64_t cols, qmv_stream st,
+                              qmv_weights** out) {
+    QMV_REQUIRE(out, QMV_ERR_INVALID_ARG, "qmv_pack_q2_blocks: out is NULL");
+    *out = nullptr;
+    QMV_REQUIRE(blocks, QMV_ERR_INVALID_ARG, "qmv_pack_q2_blocks: blocks is NULL");
+    QMV_REQUIRE(group == 64 || group == 128, QMV_ERR_INVALID_ARG,
+                "qmv_pack_q2_blocks: group must be 64 or 128 (got %d)", group);
+    QMV_REQUIRE(rows >= 1 && cols >= group && cols % group == 0, QMV_ERR_INVALID_ARG,
+                "qmv_pack_q2_blocks: need rows >= 1 and cols a positive multiple of the group (rows=%lld cols=%lld)",
+                (long long)rows, (long long)cols);
+    QMV_REQUIRE(rows <= (int64_t)1 << 30 && cols <= 32768, QMV_ERR_UNSUPPORTED,
+                "qmv_pack_q2_blocks: supports cols <= 32768 (got %lld)", (long long)cols);
+    const size_t cbytes = (size_t)rows * (size_t)(cols / 4);
+    const size_t dcount = (size_t)rows * (size_t)(cols / group);
+    std::vector<uint8_t> hc;
+    std::vector<uint16_t> hd;
+    try {
+        hc.resize(cbytes);
+        hd.resize(dcount);
+    } catch (const std::bad_alloc&) {
+        return qmv::fail(QMV_ERR_ALLOC, "qmv_pack_q2_blocks: out of host memory for %zu bytes", cbytes + 2 * dcount);
+    }
+    qmv_status s = qmv_q2_blocks_to_planar(blocks, group, rows, cols, hc.data(), hd.data());
+    if (s != QMV_OK) return s;
+    const size_t doff = (size_t)round_up((int64_t)cbytes, 256);
+    void* staging = nullptr;
+    if (cudaMalloc(&staging, doff + 2 * dcount) != cudaSuccess) {
+        cudaGetLastError();
+        return qmv::fail(QMV_ERR_ALLOC, "qmv_pack_q2_blocks: cudaMalloc of %zu staging bytes failed", doff + 2 * dcount);
+    }
+    uint8_t* dc = static_cast<uint8_t*>(staging);
+    uint16_t* dd = reinterpret_cast<uint16_t*>(static_cast<char*>(staging) + doff);
+    cudaStream_t cs = (cudaStream_t)st;
+    cudaError_t e = cudaMemcpyAsync(dc, hc.data(), cbytes, cudaMemcpyHostToDevice, cs);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dd, hd.data(), 2 * dcount, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaStreamSynchronize(cs);
+        cudaFree(staging);
+        return qmv::fail(QMV_ERR_CUDA, "qmv_pack_q2_blocks: copy to the device failed: %s", cudaGetErrorString(e));
+    }
+    s = qmv_pack_q2(dc, dd, group, rows, cols, st, out);
+    // the host arrays and the device staging copy must outlive the repack
+    e = cudaStreamSynchronize(cs);
+    cudaFree(staging);
+    if (s != QMV_OK) return s;
+    if (e != cudaSuccess) {
+        qmv_weights_free(*out);
+        *out = nullptr;
+        return qmv::fail(QMV_ERR_CUDA, "qmv_pack_q2_blocks: repack failed: %s", cudaGetErrorString(e));
+    }
     return QMV_OK;
 }
 

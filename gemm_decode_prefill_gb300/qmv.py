@@ -1,19 +1,22 @@
 """Thin Python binding of libqmv's C ABI (include/qmv.h).
 
 Argument marshalling only: every step of the computation runs in the CUDA
-kernels of libqmv.so.  PyTorch provides device memory and streams.  If the
-library has not been built, importing this module raises: there is no
-fallback path.
+kernels of libqmv.so (the one host-side step, rewriting stored Q2 blocks
+into planar arrays at load time, is the library's own C++ code).  PyTorch
+provides device memory and streams.  If the library has not been built,
+importing this module raises: there is no fallback path.
 
 Names follow the C entry points: ``qmv_pack_q8row``, ``qmv_pack_q2``,
-``qmv_q8row``, ``qmv_q2g64``, ``qmv_q2g128``, ``qmm_q8row``,
-``moe_select_topk``, ``moe_ffn_q8row``, ``qmv_check``.
+``qmv_pack_q2_blocks``, ``qmv_q2_blocks_to_planar``, ``qmv_q8row``,
+``qmv_q2g64``, ``qmv_q2g128``, ``qmm_q8row``, ``moe_select_topk``,
+``moe_ffn_q8row``, ``qmv_check``.
 """
 from __future__ import annotations
 
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +38,8 @@ _SIGS = {
     "qmv_version": ([], _I),
     "qmv_pack_q8row": ([_P, _P, _I64, _I64, _I64, _P, ctypes.POINTER(_P)], _I),
     "qmv_pack_q2": ([_P, _P, _I, _I64, _I64, _P, ctypes.POINTER(_P)], _I),
+    "qmv_q2_blocks_to_planar": ([_P, _I, _I64, _I64, _P, _P], _I),
+    "qmv_pack_q2_blocks": ([_P, _I, _I64, _I64, _P, ctypes.POINTER(_P)], _I),
     "qmv_weights_info": ([_P, ctypes.POINTER(_I), ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                           ctypes.POINTER(_I64), ctypes.POINTER(_I64)], _I),
     "qmv_weights_free": ([_P], _I),
@@ -171,6 +176,38 @@ def qmv_pack_q2(codes: torch.Tensor, d_bits: torch.Tensor, group: int, stream=No
     h = ctypes.c_void_p()
     _check(_lib.qmv_pack_q2(cp, dp, int(group), rows, cols, _stream(stream), ctypes.byref(h)),
            "qmv_pack_q2")
+    return _wrap(h)
+
+
+def _q2_blocks_shape(blocks, group: int):
+    if group not in (64, 128):
+        raise ValueError("group must be 64 or 128")
+    if not isinstance(blocks, np.ndarray) or blocks.dtype != np.uint8 or blocks.ndim != 2:
+        raise TypeError("blocks must be a 2-D uint8 numpy array [rows][cols/group * (2 + group/4)]")
+    bs = 2 + group // 4
+    if blocks.shape[1] % bs:
+        raise ValueError(f"a row of blocks must be a multiple of {bs} bytes")
+    return np.ascontiguousarray(blocks), blocks.shape[0], blocks.shape[1] // bs * group
+
+
+def qmv_q2_blocks_to_planar(blocks: np.ndarray, group: int):
+    """Block form (host uint8 [rows][nb * (2 + group/4)]) -> planar (codes
+    uint8 [rows][cols/4], d f16 bit patterns uint16 [rows][cols/group]),
+    rewritten by the library's host code."""
+    blocks, rows, cols = _q2_blocks_shape(blocks, group)
+    codes = np.empty((rows, cols // 4), np.uint8)
+    d = np.empty((rows, cols // group), np.uint16)
+    _check(_lib.qmv_q2_blocks_to_planar(blocks.ctypes.data, int(group), rows, cols, codes.ctypes.data,
+                                        d.ctypes.data), "qmv_q2_blocks_to_planar")
+    return codes, d
+
+
+def qmv_pack_q2_blocks(blocks: np.ndarray, group: int, stream=None) -> Weights:
+    """Packs Q2 weights given in the block form in host memory."""
+    blocks, rows, cols = _q2_blocks_shape(blocks, group)
+    h = ctypes.c_void_p()
+    _check(_lib.qmv_pack_q2_blocks(blocks.ctypes.data, int(group), rows, cols, _stream(stream), ctypes.byref(h)),
+           "qmv_pack_q2_blocks")
     return _wrap(h)
 
 

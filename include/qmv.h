@@ -114,6 +114,33 @@ QMV_API qmv_status qmv_pack_q2(const uint8_t *codes, const uint16_t *d, int grou
                        int64_t rows, int64_t cols, qmv_stream st,
                        qmv_weights **out);
 
+/* Q2 weights in the block form, the form they are stored in: row by row,
+ * one block per group of `group` weights, each block 2 + group/4 bytes
+ * (18 for g64, 34 for g128):
+ *   { f16 d (bit pattern, little-endian); uint8 qs[group/4] }
+ * with code k of the block at qs[k/4], bits 2(k%4), weight d * (q - 1).
+ * The footprints and the member names d, qs are those of qxmx_gpu.cpp
+ * (`upload_q2`, `qx_block_q2` / `qx_block_q2_g128`); the field order,
+ * d first, is an assumption, since the struct's declaration is not given.
+ *
+ * qmv_q2_blocks_to_planar rewrites blocks [rows][cols/group] into the
+ * planar arrays qmv_pack_q2 takes: codes [rows][cols/4] and d
+ * [rows][cols/group].  All three pointers are HOST memory, owned by the
+ * caller; pure host code (no CUDA call), QMV_ERR_INVALID_ARG on a null
+ * pointer, a group other than 64 / 128, rows < 1 or cols not a positive
+ * multiple of the group. */
+QMV_API qmv_status qmv_q2_blocks_to_planar(const void *blocks, int group, int64_t rows,
+                                   int64_t cols, uint8_t *codes, uint16_t *d);
+
+/* Packs Q2 weights given in the block form in HOST memory (as read from a
+ * weight file): rewrites them on the host, copies the planar arrays to a
+ * device staging buffer on `st`, packs them as qmv_pack_q2 does and
+ * synchronizes `st` before returning, so `blocks` may be released as soon
+ * as the call returns.  Same argument rules and errors as qmv_pack_q2, plus
+ * QMV_ERR_ALLOC when the host or device staging memory cannot be had. */
+QMV_API qmv_status qmv_pack_q2_blocks(const void *blocks, int group, int64_t rows, int64_t cols,
+                              qmv_stream st, qmv_weights **out);
+
 /* Describes a handle (host out-pointers, each may be NULL). */
 QMV_API qmv_status qmv_weights_info(const qmv_weights *w, int *format, int64_t *experts,
                             int64_t *rows, int64_t *cols, int64_t *device_bytes);

@@ -56,6 +56,8 @@ def _load():
     lib.oracle_round_bf16.restype = ctypes.c_float
     lib.oracle_threads.argtypes = [I, I64]
     lib.oracle_threads.restype = I
+    lib.oracle_q2_blocks.argtypes = [P, I, P, I64, I64, P, I]
+    lib.oracle_q2_blocks.restype = I
     lib.oracle_q8row.argtypes = [P, P, P, I64, I64, P, P, I]
     lib.oracle_q8row.restype = I
     lib.oracle_qmm.argtypes = [P, P, P, I64, I64, I64, P, P, I]
@@ -144,6 +146,26 @@ def q2(codes, d_bits, group: int, x, nthreads: int = 0, with_mag: bool = False):
     if rc < 0:
         raise ValueError("oracle_q2: bad group/cols")
     return (y, mag) if with_mag else y
+
+
+def q2_blocks(blocks, group: int, x, nthreads: int = 0):
+    """Q2 group GEMV in fp64 from the block form: blocks uint8
+    [rows][cols/group * (2 + group/4)], each block {f16 d little-endian;
+    qs[group/4]}."""
+    lib = _load()
+    if group not in (64, 128):
+        raise ValueError("oracle_q2_blocks: group must be 64 or 128")
+    blocks, bp = _c(blocks, np.uint8)
+    bsize = 2 + group // 4
+    rows = blocks.shape[0]
+    assert blocks.shape[1] % bsize == 0
+    cols = blocks.shape[1] // bsize * group
+    x, xp = _c(x, np.float32)
+    assert x.shape == (cols,)
+    y = np.empty(rows, np.float64)
+    if lib.oracle_q2_blocks(bp, group, xp, rows, cols, y.ctypes.data, nthreads) < 0:
+        raise ValueError("oracle_q2_blocks: bad group/cols")
+    return y
 
 
 def select(logits, top_k: int, renorm: bool, sgw=None, x=None, sg_logit=None):

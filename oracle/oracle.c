@@ -278,6 +278,58 @@ int oracle_q2(const uint8_t *codes, const uint16_t *d, int group,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Q2 in the block form (how the weights are stored): row by row, one      */
+/* block per group, {f16 d; u8 qs[group/4]}, 2 + group/4 bytes (18 / 34).   */
+/* [P1] `upload_q2` gives the footprints and the member names d, qs; the     */
+/* field order (d first, its two bytes little-endian) is a reading, since   */
+/* the struct's declaration is not on the pages.  Code kk of a block is at  */
+/* qs[kk/4], bits 2(kk%4), weight d*(q-1) (`dequant_embd`).  The sums run   */
+/* in the same order as oracle_q2.                                          */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    const uint8_t *blocks;
+    const float *x;
+    int group;
+    int64_t cols;
+    double *y;
+} q2b_ctx;
+
+static void q2b_rows(void *p, int64_t r0, int64_t r1)
+{
+    q2b_ctx *c = (q2b_ctx *)p;
+    int64_t nblk = c->cols / c->group;
+    int64_t bsize = 2 + c->group / 4;
+    for (int64_t m = r0; m < r1; ++m) {
+        double ym = 0.0;
+        for (int64_t b = 0; b < nblk; ++b) {
+            const uint8_t *blk = c->blocks + (m * nblk + b) * bsize;
+            uint16_t dbits = (uint16_t)((unsigned)blk[0] | ((unsigned)blk[1] << 8));
+            const uint8_t *qs = blk + 2;
+            double dg = oracle_f16_to_f64(dbits);
+            double s = 0.0;
+            for (int64_t kk = 0; kk < c->group; ++kk) {
+                int q = (qs[kk / 4] >> (2 * (kk % 4))) & 3;
+                s += (double)(q - 1) * (double)c->x[b * c->group + kk];
+            }
+            ym += dg * s;
+        }
+        c->y[m] = ym;
+    }
+}
+
+/* blocks: [rows][cols/group] blocks as above; x: [cols]; group is 64 or 128
+ * and divides cols.  Returns the number of threads used, or -1. */
+int oracle_q2_blocks(const uint8_t *blocks, int group, const float *x,
+                     int64_t rows, int64_t cols, double *y, int nthreads)
+{
+    if (group != 64 && group != 128) return -1;
+    if (cols % group) return -1;
+    q2b_ctx c = {blocks, x, group, cols, y};
+    return run_rows(q2b_rows, &c, rows, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
 /* MoE router select                     [P2] `moe_select_sg`, `moe_select` */
 /*  - softmax over all n logits: w_j = exp(l_j - max) / sum_all exp(l - max) */
 /*  - k rounds of argmax over the not-yet-chosen experts; equal values:     */

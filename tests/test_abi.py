@@ -26,7 +26,8 @@ def _declared():
 def test_header_declares_the_hot_path():
     names = _declared()
     for n in ["qmv_q8row", "qmv_q2g64", "qmv_q2g128", "qmm_q8row", "moe_select_topk",
-              "moe_ffn_q8row", "qmv_pack_q8row", "qmv_pack_q2"]:
+              "moe_ffn_q8row", "qmv_pack_q8row", "qmv_pack_q2", "qmv_pack_q2_blocks",
+              "qmv_q2_blocks_to_planar"]:
         assert n in names
 
 
@@ -73,4 +74,53 @@ def test_shape_rules_are_checked_before_cuda(lib):
     assert L.moe_select_topk(fake, 2000, 2, 1, None, None, 0, None, fake, fake, None) == 1
     assert L.moe_select_topk(fake, 8, 9, 1, None, None, 0, None, fake, fake, None) == 1
     assert L.moe_select_topk(fake, 8, 0, 1, None, None, 0, None, fake, fake, None) == 1
+    assert h.value is None
+
+
+# ------------------------------------------- Q2 block form (host code only)
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_blocks_to_planar_matches_field_split(lib, group):
+    """The library's host rewrite of stored blocks equals a numpy split of
+    the fields, and the oracle gives the same result from either form."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(81 + group)
+    rows, cols = 33, 5 * group
+    nb, qb = cols // group, group // 4
+    blocks = rng.integers(0, 256, size=(rows, nb, 2 + qb), dtype=np.uint8)
+    blocks[:, :, 1] &= 0x7B          # finite d
+    codes, d = lib.qmv_q2_blocks_to_planar(blocks.reshape(rows, -1), group)
+    assert np.array_equal(codes, blocks[:, :, 2:].reshape(rows, cols // 4))
+    assert np.array_equal(d, blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    x = rng.standard_normal(cols).astype(np.float32)
+    assert np.array_equal(oracle.q2_blocks(blocks.reshape(rows, -1), group, x), oracle.q2(codes, d, group, x))
+
+
+def test_q2_blocks_worked_fixture_through_the_library(lib):
+    import numpy as np
+    import oracle
+    g = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "q2_blocks_g64_worked.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            g[k.strip()] = v.strip()
+    blocks = np.frombuffer(bytes.fromhex(g["blocks_hex"]), np.uint8).reshape(1, -1)
+    codes, d = lib.qmv_q2_blocks_to_planar(blocks, 64)
+    assert d.tolist() == [[0x3800, 0x4000]]
+    assert oracle.q2(codes, d, 64, np.ones(128, np.float32)).tolist() == [float(g["y"])]
+
+
+def test_q2_block_arguments_are_checked_before_cuda(lib):
+    L = lib._lib
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(4096)  # never dereferenced: validation fails first
+    assert L.qmv_q2_blocks_to_planar(None, 64, 1, 64, fake, fake) == 1
+    assert L.qmv_q2_blocks_to_planar(fake, 32, 1, 64, fake, fake) == 1     # group
+    assert L.qmv_q2_blocks_to_planar(fake, 64, 1, 96, fake, fake) == 1     # cols % group
+    assert L.qmv_q2_blocks_to_planar(fake, 64, 0, 64, fake, fake) == 1     # rows
+    assert L.qmv_pack_q2_blocks(None, 64, 1, 64, None, ctypes.byref(h)) == 1
+    assert L.qmv_pack_q2_blocks(fake, 48, 1, 64, None, ctypes.byref(h)) == 1
+    assert L.qmv_pack_q2_blocks(fake, 128, 1, 65536, None, ctypes.byref(h)) == 2  # too wide
+    assert L.qmv_pack_q2_blocks(fake, 64, 1, 64, None, None) == 1
     assert h.value is None

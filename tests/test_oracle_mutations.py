@@ -24,6 +24,11 @@ MUTATIONS = [
     ("moe_silu_sign", "double a = g / (1.0 + exp(-g)) * u;", "double a = g / (1.0 + exp(g)) * u;"),
     ("moe_weight_dropped", "acc += w[s] * rsd * sd;", "acc += rsd * sd;"),
     ("bf16_round_truncates", "if (lower > half || (lower == half && odd))", "if (0)"),
+    ("q2_blocks_d_big_endian", "(uint16_t)((unsigned)blk[0] | ((unsigned)blk[1] << 8))",
+     "(uint16_t)((unsigned)blk[1] | ((unsigned)blk[0] << 8))"),
+    ("q2_blocks_d_after_qs", "const uint8_t *qs = blk + 2;\n            double dg = oracle_f16_to_f64(dbits);",
+     "const uint8_t *qs = blk;\n            dbits = (uint16_t)((unsigned)blk[bsize - 2] | ((unsigned)blk[bsize - 1] << 8));\n"
+     "            double dg = oracle_f16_to_f64(dbits);"),
 ]
 
 

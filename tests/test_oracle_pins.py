@@ -67,6 +67,35 @@ def test_golden_q2(name):
     assert y.tolist() == y_ref
 
 
+@pytest.mark.parametrize("name", ["q2_blocks_g64_worked.txt", "q2_blocks_g128_worked.txt"])
+def test_golden_q2_blocks(name):
+    g = _fixture(name)
+    group, rows, cols = int(g["group"]), int(g["rows"]), int(g["cols"])
+    blocks = np.frombuffer(bytes.fromhex(g["blocks_hex"]), np.uint8).reshape(rows, -1)
+    assert g["x"] == "ones"
+    y = oracle.q2_blocks(blocks, group, np.ones(cols, np.float32))
+    assert y.tolist() == _nums(g["y"])
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_blocks_reader_equals_planar_reader(group):
+    """The block reader and the planar reader agree bit for bit (same sums,
+    same order) on random weights, with the block fields split out by numpy
+    slicing: pins the block reader's field offsets and d's byte order
+    against the planar reader, which the hand-worked fixtures pin."""
+    rng = np.random.default_rng(71 + group)
+    rows, cols = 7, 4 * group
+    nb, qb = cols // group, group // 4
+    blocks = rng.integers(0, 256, size=(rows, nb, 2 + qb), dtype=np.uint8)
+    blocks[:, :, 1] &= 0x7B          # keep d finite (exponent field below 0x1F)
+    x = rng.standard_normal(cols).astype(np.float32)
+    codes = blocks[:, :, 2:].reshape(rows, cols // 4)
+    d = (blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    y_blocks = oracle.q2_blocks(blocks.reshape(rows, -1), group, x)
+    y_planar = oracle.q2(codes, d, group, x)
+    assert np.array_equal(y_blocks, y_planar)
+
+
 def test_golden_select():
     g = _fixture("select_worked.txt")
     logits = np.array(_nums(g["logits"]), np.float32)
