@@ -56,6 +56,10 @@ def _load():
     lib.oracle_round_bf16.restype = ctypes.c_float
     lib.oracle_threads.argtypes = [I, I64]
     lib.oracle_threads.restype = I
+    lib.oracle_quant_act.argtypes = [P, I64, I, P, P, ctypes.POINTER(ctypes.c_float)]
+    lib.oracle_quant_act.restype = I
+    lib.oracle_q2_i8.argtypes = [P, P, I, P, P, ctypes.c_float, I64, I64, P, P, I]
+    lib.oracle_q2_i8.restype = I
     lib.oracle_q2_blocks.argtypes = [P, I, P, I64, I64, P, I]
     lib.oracle_q2_blocks.restype = I
     lib.oracle_q8row.argtypes = [P, P, P, I64, I64, P, P, I]
@@ -166,6 +170,39 @@ def q2_blocks(blocks, group: int, x, nthreads: int = 0):
     if lib.oracle_q2_blocks(bp, group, xp, rows, cols, y.ctypes.data, nthreads) < 0:
         raise ValueError("oracle_q2_blocks: bad group/cols")
     return y
+
+
+def quant_act(x, group: int):
+    """Per-token int8 quantisation of an activation vector.  Returns
+    (a int8 [cols], sum_a int32 [cols/group], act_scale float32)."""
+    lib = _load()
+    x, xp = _c(x, np.float32)
+    cols = x.shape[0]
+    a = np.empty(cols, np.int8)
+    sa = np.empty(cols // group, np.int32)
+    sc = ctypes.c_float()
+    if lib.oracle_quant_act(xp, cols, group, a.ctypes.data, sa.ctypes.data, ctypes.byref(sc)) < 0:
+        raise ValueError("oracle_quant_act: bad group/cols")
+    return a, sa, np.float32(sc.value)
+
+
+def q2_i8(codes, d_bits, group: int, a, sum_a, act_scale, nthreads: int = 0, with_mag: bool = False):
+    """Q2 group GEMV on int8 activations (a, sum_a, act_scale from quant_act), fp64."""
+    lib = _load()
+    codes, cp = _c(codes, np.uint8)
+    rows = codes.shape[0]
+    cols = codes.shape[1] * 4
+    d_bits, dp = _c(d_bits, np.uint16)
+    a, ap = _c(a, np.int8)
+    sum_a, sp = _c(sum_a, np.int32)
+    assert d_bits.shape == (rows, cols // group) and a.shape == (cols,) and sum_a.shape == (cols // group,)
+    y = np.empty(rows, np.float64)
+    mag = np.empty(rows, np.float64) if with_mag else None
+    rc = lib.oracle_q2_i8(cp, dp, group, ap, sp, ctypes.c_float(float(act_scale)), rows, cols, y.ctypes.data,
+                          mag.ctypes.data if with_mag else None, nthreads)
+    if rc < 0:
+        raise ValueError("oracle_q2_i8: bad group/cols")
+    return (y, mag) if with_mag else y
 
 
 def select(logits, top_k: int, renorm: bool, sgw=None, x=None, sg_logit=None):

@@ -330,6 +330,100 @@ int oracle_q2_blocks(const uint8_t *blocks, int group, const float *x,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Q2 on int8 activations [P1]: the quantise half of `gpu_rmsnorm_quant`    */
+/* (the norm is a separate step: x is the activation as given) and the      */
+/* integer product of `gemv_dpas8` with `gemv_reduce`.                      */
+/*   act_scale = amax / 127            (f32 division, amax = max |x_k|)     */
+/*   a_k = clamp(round(x_k * (1 / act_scale)), -128, 127)                   */
+/*         the reciprocal and the product in f32, round() taking halfway    */
+/*         cases away from zero (C / SYCL round), a_k = 0 when amax = 0     */
+/*   sum_a[g] = sum_{k in g} a_k                                            */
+/*   y[m] = act_scale * sum_g d[m,g] * (sum_{k in g} q[m,k]*a_k - sum_a[g]) */
+/* Here floating point decides integers (the a_k), so those steps are taken */
+/* in f32 exactly as the page takes them; the sums are exact integers and   */
+/* the rest is fp64.                                                        */
+/* ------------------------------------------------------------------------ */
+
+/* x: [cols]; a: [cols] out; sum_a: [cols/group] out; *act_scale out.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_quant_act(const float *x, int64_t cols, int group, int8_t *a,
+                     int32_t *sum_a, float *act_scale)
+{
+    if ((group != 64 && group != 128) || cols % group) return -1;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < cols; ++k) {
+        float v = fabsf(x[k]);
+        if (v > amax) amax = v;
+    }
+    float sc = amax / 127.0f;
+    float invq = sc > 0.0f ? 1.0f / sc : 0.0f;
+    for (int64_t g = 0; g < cols / group; ++g) {
+        int32_t sa = 0;
+        for (int64_t kk = 0; kk < group; ++kk) {
+            int64_t k = g * group + kk;
+            float ov = x[k] * invq;
+            long v = lroundf(ov);
+            if (v < -128) v = -128;
+            if (v > 127) v = 127;
+            a[k] = (int8_t)v;
+            sa += (int32_t)v;
+        }
+        sum_a[g] = sa;
+    }
+    *act_scale = sc;
+    return 0;
+}
+
+typedef struct {
+    const uint8_t *codes;
+    const uint16_t *d;
+    const int8_t *a;
+    const int32_t *sum_a;
+    double act_scale;
+    int group;
+    int64_t cols;
+    double *y, *mag;
+} q2i8_ctx;
+
+static void q2i8_rows(void *p, int64_t r0, int64_t r1)
+{
+    q2i8_ctx *c = (q2i8_ctx *)p;
+    int64_t ngrp = c->cols / c->group;
+    int64_t row_bytes = c->cols / 4;
+    for (int64_t m = r0; m < r1; ++m) {
+        const uint8_t *row = c->codes + m * row_bytes;
+        double ym = 0.0, am = 0.0;
+        for (int64_t g = 0; g < ngrp; ++g) {
+            int64_t p = 0, pa = 0;
+            for (int64_t kk = 0; kk < c->group; ++kk) {
+                int64_t k = g * c->group + kk;
+                int q = (row[k / 4] >> (2 * (k % 4))) & 3;
+                int w1 = q - 1, ak = c->a[k];
+                p += (int64_t)q * ak;
+                pa += (int64_t)(w1 < 0 ? -w1 : w1) * (ak < 0 ? -ak : ak);
+            }
+            double dg = oracle_f16_to_f64(c->d[m * ngrp + g]);
+            ym += dg * (double)(p - c->sum_a[g]);
+            am += fabs(dg) * (double)pa;
+        }
+        c->y[m] = c->act_scale * ym;
+        if (c->mag) c->mag[m] = fabs(c->act_scale) * am;
+    }
+}
+
+/* codes, d, group as oracle_q2; a, sum_a, act_scale from oracle_quant_act.
+ * mag[m] = act_scale * sum_g |d| * sum_k |(q-1) a_k|, may be NULL. */
+int oracle_q2_i8(const uint8_t *codes, const uint16_t *d, int group,
+                 const int8_t *a, const int32_t *sum_a, float act_scale,
+                 int64_t rows, int64_t cols, double *y, double *mag,
+                 int nthreads)
+{
+    if ((group != 64 && group != 128) || cols % group) return -1;
+    q2i8_ctx c = {codes, d, a, sum_a, (double)act_scale, group, cols, y, mag};
+    return run_rows(q2i8_rows, &c, rows, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
 /* MoE router select                     [P2] `moe_select_sg`, `moe_select` */
 /*  - softmax over all n logits: w_j = exp(l_j - max) / sum_all exp(l - max) */
 /*  - k rounds of argmax over the not-yet-chosen experts; equal values:     */

@@ -11,9 +11,13 @@ SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 # (name, text in oracle.c, replacement)
 MUTATIONS = [
-    ("q2_bit_order_reversed", "(row[k / 4] >> (2 * (k % 4))) & 3", "(row[k / 4] >> (2 * (3 - k % 4))) & 3"),
+    ("q2_bit_order_reversed", "(row[k / 4] >> (2 * (k % 4))) & 3;\n                double t",
+     "(row[k / 4] >> (2 * (3 - k % 4))) & 3;\n                double t"),
+    ("q2_i8_bit_order_reversed", "(row[k / 4] >> (2 * (k % 4))) & 3;\n                int w1",
+     "(row[k / 4] >> (2 * (3 - k % 4))) & 3;\n                int w1"),
     ("q2_offset_dropped", "(double)(q - 1) * (double)c->x[k]", "(double)(q) * (double)c->x[k]"),
-    ("q2_wrong_group_scale", "c->d[m * ngrp + g]", "c->d[m * ngrp]"),
+    ("q2_wrong_group_scale", "c->d[m * ngrp + g]);\n            double s = 0.0",
+     "c->d[m * ngrp]);\n            double s = 0.0"),
     ("f16_subnormal_scale", "ldexp((double)m, -24)", "ldexp((double)m, -14)"),
     ("q8_row_scale_dropped", "c->y[o] = (double)c->rs[o] * s;", "c->y[o] = s;"),
     ("qmm_transposed_output", "c->y[b * c->rows + o] = (double)c->rs[o] * s;", "c->y[o * c->nb + b] = (double)c->rs[o] * s;"),
@@ -24,6 +28,9 @@ MUTATIONS = [
     ("moe_silu_sign", "double a = g / (1.0 + exp(-g)) * u;", "double a = g / (1.0 + exp(g)) * u;"),
     ("moe_weight_dropped", "acc += w[s] * rsd * sd;", "acc += rsd * sd;"),
     ("bf16_round_truncates", "if (lower > half || (lower == half && odd))", "if (0)"),
+    ("quant_round_half_even", "long v = lroundf(ov);", "long v = lrintf(ov);"),
+    ("quant_scale_255", "float sc = amax / 127.0f;", "float sc = amax / 255.0f;"),
+    ("q2_i8_sum_a_dropped", "ym += dg * (double)(p - c->sum_a[g]);", "ym += dg * (double)p;"),
     ("q2_blocks_d_big_endian", "(uint16_t)((unsigned)blk[0] | ((unsigned)blk[1] << 8))",
      "(uint16_t)((unsigned)blk[1] | ((unsigned)blk[0] << 8))"),
     ("q2_blocks_d_after_qs", "const uint8_t *qs = blk + 2;\n            double dg = oracle_f16_to_f64(dbits);",

@@ -96,6 +96,70 @@ def test_q2_blocks_reader_equals_planar_reader(group):
     assert np.array_equal(y_blocks, y_planar)
 
 
+# ------------------------------------------- Q2 on int8 activations
+
+def test_golden_q2_i8():
+    group, codes, d, x, y_ref = _q2_fixture("q2_i8_worked.txt")
+    g = _fixture("q2_i8_worked.txt")
+    a, sa, sc = oracle.quant_act(x, group)
+    head = _nums(g["a_head"], int)
+    assert a[:len(head)].tolist() == head and not a[len(head):].any()
+    assert sa.tolist() == _nums(g["sum_a"], int)
+    assert float(sc) == float(g["act_scale"])
+    assert oracle.q2_i8(codes, d, group, a, sa, sc).tolist() == y_ref
+
+
+def test_quant_act_properties():
+    rng = np.random.default_rng(91)
+    x = rng.standard_normal(1024).astype(np.float32)
+    a, sa, sc = oracle.quant_act(x, 64)
+    assert np.abs(a.astype(int)).max() == 127
+    assert abs(int(a[np.argmax(np.abs(x))])) == 127
+    assert sa.tolist() == a.astype(np.int64).reshape(-1, 64).sum(axis=1).tolist()
+    # sign symmetry (round half away from zero is odd)
+    a_neg, _, sc_neg = oracle.quant_act(-x, 64)
+    assert np.array_equal(a_neg, -a) and sc_neg == sc
+    # a power-of-two rescale of x changes act_scale exactly and no code
+    for k in (-20, -3, 5, 30):
+        a_k, _, sc_k = oracle.quant_act((x * np.float32(2.0 ** k)).astype(np.float32), 64)
+        assert np.array_equal(a_k, a) and float(sc_k) == float(sc) * 2.0 ** k
+    # every code is within half a step of x / act_scale
+    assert np.all(np.abs(a - x.astype(np.float64) / float(sc)) <= 0.5 + 1e-5)
+    # zero activation
+    z, zs, zsc = oracle.quant_act(np.zeros(128, np.float32), 128)
+    assert not z.any() and not zs.any() and zsc == 0
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_i8_equals_dense_product_of_dequantised_operands(group):
+    rng = np.random.default_rng(92 + group)
+    rows, cols = 9, 3 * group
+    codes = rng.integers(0, 256, size=(rows, cols // 4), dtype=np.uint8)
+    d = rng.uniform(0.005, 0.05, size=(rows, cols // group)).astype(np.float16).view(np.uint16)
+    x = rng.standard_normal(cols).astype(np.float32)
+    a, sa, sc = oracle.quant_act(x, group)
+    q = np.stack([(codes >> (2 * j)) & 3 for j in range(4)], axis=-1).reshape(rows, cols).astype(np.float64)
+    w = (q - 1.0) * np.repeat(d.view(np.float16).astype(np.float64), group, axis=1)
+    dense = w @ (a.astype(np.float64) * float(sc))
+    np.testing.assert_allclose(oracle.q2_i8(codes, d, group, a, sa, sc), dense, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q2_i8_reduces_to_q2_when_quantisation_is_exact(group):
+    """Integer activations with max |x| = 127 quantise to themselves
+    (act_scale = 1), and the int8 path must then equal the plain Q2 product
+    bit for bit."""
+    rng = np.random.default_rng(93 + group)
+    rows, cols = 11, 2 * group
+    codes = rng.integers(0, 256, size=(rows, cols // 4), dtype=np.uint8)
+    d = rng.uniform(0.005, 0.05, size=(rows, cols // group)).astype(np.float16).view(np.uint16)
+    x = rng.integers(-127, 128, size=cols).astype(np.float32)
+    x[5] = 127.0
+    a, sa, sc = oracle.quant_act(x, group)
+    assert sc == 1 and np.array_equal(a.astype(np.float32), x)
+    assert np.array_equal(oracle.q2_i8(codes, d, group, a, sa, sc), oracle.q2(codes, d, group, x))
+
+
 def test_golden_select():
     g = _fixture("select_worked.txt")
     logits = np.array(_nums(g["logits"]), np.float32)
